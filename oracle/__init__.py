@@ -17,6 +17,8 @@ Pinning status (what each function is checked against in ``tests/``):
 * ``mlp_geglu``: gelu pins + composition from pinned linear pieces -- pinned.
 * ``materialize_f32``/``materialize_bf16``: per-element recomputation with
   Python's correctly rounded float ops and numpy float32, passthrough -- pinned.
+* ``f64_to_bf16``/``round_bf16``: exact rational rounding, torch's fp32 cast
+  on fp32-representable values -- pinned.
 * ``rel_frobenius``: zero at passthrough, closed form for an added E -- pinned.
 * ``band_of_layer``: G = L identity, G = 1 constant -- pinned for those G;
   the contiguous-band formula for 1 < G < L is a reading (parity unpinned
@@ -84,6 +86,7 @@ def _configure(L):
     L.orc_materialize_f32.argtypes = [_u16p(), _f32p(), vp, vp, i64, i64, i64, _f32p()]
     L.orc_materialize_bf16.argtypes = [_u16p(), _f32p(), vp, vp, i64, i64, i64, _u16p()]
     L.orc_f32_to_bf16.argtypes = [_f32p(), i64, _u16p()]
+    L.orc_f64_to_bf16.argtypes = [_f64p(), i64, _u16p()]
     L.orc_rel_frobenius.argtypes = [_f64p(), _u16p(), _f32p(), vp, vp, i64, i64, i64]
     L.orc_rel_frobenius.restype = C.c_double
     L.orc_band_of_layer.argtypes = [i64, i64, i64]
@@ -280,6 +283,19 @@ def f32_to_bf16(a) -> np.ndarray:
     b = np.empty(a.shape, np.uint16)
     lib().orc_f32_to_bf16(a.reshape(-1), a.size, b.reshape(-1))
     return b
+
+
+def f64_to_bf16(a) -> np.ndarray:
+    """fp64 -> bf16 bits with one correct rounding (RNE)."""
+    a = np.ascontiguousarray(np.asarray(a, np.float64))
+    b = np.empty(a.shape, np.uint16)
+    lib().orc_f64_to_bf16(a.reshape(-1), a.size, b.reshape(-1))
+    return b
+
+
+def round_bf16(a) -> np.ndarray:
+    """The fp64 values after the method's final cast to bf16, as float64."""
+    return bf16_bits_to_f64(f64_to_bf16(a))
 
 
 def rel_frobenius(W, theta) -> float:

@@ -310,6 +310,36 @@ void orc_f32_to_bf16(const float *a, int64_t n, uint16_t *b)
 }
 
 /*
+ * fp64 -> bf16 bits, one correct rounding (nearest, ties to even).  The
+ * method ends with a cast of the fp32 combine to the output dtype
+ * ("In-kernel reconstruction", custom-op path and "The GEMM path"); for a
+ * bf16 output the reference value is the exact result after that cast.
+ * Rounds the 53-bit significand to 8 bits on the bit pattern; the kept value
+ * is then exact in fp32.  Normal range only (tiny values below 2^-126 are
+ * outside what this library produces); zero and sign are kept.
+ */
+void orc_f64_to_bf16(const double *a, int64_t n, uint16_t *b)
+{
+    for (int64_t j = 0; j < n; ++j) {
+        uint64_t u;
+        memcpy(&u, &a[j], sizeof u);
+        if ((u & 0x7fffffffffffffffull) > 0x7ff0000000000000ull) { /* NaN */
+            b[j] = 0x7fc0u;
+            continue;
+        }
+        const uint64_t lsb = (u >> 45) & 1ull;
+        u += (1ull << 44) - 1ull + lsb;
+        u &= ~((1ull << 45) - 1ull);
+        double d;
+        memcpy(&d, &u, sizeof d);
+        float f = (float)d; /* exact: at most 8 significant bits */
+        uint32_t fb;
+        memcpy(&fb, &f, sizeof fb);
+        b[j] = (uint16_t)(fb >> 16);
+    }
+}
+
+/*
  * relative_frobenius_error ("What weightless inference costs",
  * "Reconstruction fidelity"):
  *   ||W - (diag(s) W0 + U V^T)||_F / ||W||_F,  W [out, in] given in fp64.

@@ -36,6 +36,7 @@ MUTANTS = {
     "mat_k_descending": ("for (int64_t k = 0; k < r; ++k)\n                d = fmaf(bf_f32(U[o * r + k]), bf_f32(V[i * r + k]), d);",
                          "for (int64_t k = r - 1; k >= 0; --k)\n                d = fmaf(bf_f32(U[o * r + k]), bf_f32(V[i * r + k]), d);"),
     "bf16_ties_away": ("u += 0x7fffu + lsb;", "u += 0x8000u;"),
+    "f64_bf16_truncate": ("u += (1ull << 44) - 1ull + lsb;", "u += 0ull;"),
     "band_round": ("return (l * G) / L;", "return (l * G + L - 1) / L;"),
     "frob_no_sqrt": ("return sqrt(num) / sqrt(den);", "return num / den;"),
 }

@@ -324,3 +324,43 @@ def test_band_of_layer(orc):
     assert orc.band_of_layer(26, 26, 1) == -1
     assert orc.band_of_layer(0, 26, 27) == -1
     assert orc.band_of_layer(-1, 26, 1) == -1
+
+
+def _round_bf16_exact(v: float) -> float:
+    """Exact rational rounding of a double to 8 significant bits (RNE)."""
+    q = Fraction(v)
+    if q == 0:
+        return 0.0
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = math.floor(math.log2(a))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    m = a / Fraction(2) ** (e - 7)             # in [2^7, 2^8)
+    fl = m.numerator // m.denominator
+    rem = m - fl
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * float(Fraction(fl) * Fraction(2) ** (e - 7))
+
+
+def test_f64_to_bf16_exact_rounding(orc):
+    rng = np.random.default_rng(4)
+    v = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-6, 6, 3000),
+                        [0.0, -0.0, 1.0, -1.0]])
+    # exact midpoints between bf16 neighbours (ties) and one ulp of fp64 off them
+    base = (np.arange(1, 200, dtype=np.float64) / 128.0) * 4.0
+    mids = base + 2.0 ** -6 * 0.5 * (base / 4.0 >= 1) + 0.0
+    v = np.concatenate([v, mids, np.nextafter(mids, np.inf), np.nextafter(mids, -np.inf)])
+    got = orc.round_bf16(v)
+    want = np.array([_round_bf16_exact(float(a)) for a in v])
+    assert np.array_equal(got, want)
+
+
+def test_f64_to_bf16_agrees_with_torch_on_fp32_values(orc):
+    rng = np.random.default_rng(5)
+    a32 = rng.standard_normal(5000).astype(np.float32)
+    want = wl_synth.bf16_bits(torch.from_numpy(a32).to(torch.bfloat16))
+    assert np.array_equal(orc.f64_to_bf16(a32.astype(np.float64)), want)
