@@ -1,0 +1,367 @@
+#!/usr/bin/env python3
+"""Benchmark of the weightless linear projection path on GB300.
+
+One step = one pass of a Gemma-3-1B-shaped decoder layer stack at decode
+(T = 1): per layer fused Q/K/V (1152 -> 1024/256/256), O (1024 -> 1152) and
+the fused GeGLU MLP (1152 -> 6912 -> 1152), rank r = 4, bf16, seeded synthetic
+weights.  The stack has 26 layers with one W0 per layer (G = 26), so every
+step streams 1.4 GB of distinct weights: far larger than L2 (no flush needed;
+each layer's weights are cold when read).
+
+value = algorithmic bytes of the step / device time of the step (GB/s).
+Also reported: us per token per layer, the roofline of the dominant kernel
+(the fused MLP), the end-to-end rate through the public API with host
+buffers, and the fp64 CPU oracle on the host cores as a baseline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wl|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L_LAYERS = 26
+SHAPES = dict(hidden=1152, q=1024, kv=256, inter=6912)
+METRIC = "weightless-linear HBM GB/s (T=1) & TFLOP/s (T=2048) vs roofline; µs/token/layer"
+
+
+def proj_list(shapes):
+    h, q, kv, i = shapes["hidden"], shapes["q"], shapes["kv"], shapes["inter"]
+    return [(h, q), (h, kv), (h, kv), (q, h), (h, i), (h, i), (i, h)]  # (in, out)
+
+
+def layer_bytes(shapes, T, r):
+    """Algorithmic HBM bytes of one layer: W0 (2 B/elem), s (4 B/row),
+    U and V (2 B/elem), every projection's input and output activations."""
+    b = 0
+    for inp, out in proj_list(shapes):
+        b += 2 * out * inp + 4 * out + 2 * r * (inp + out) + 2 * T * (inp + out)
+    return b
+
+
+def mlp_bytes(shapes, T, r):
+    h, i = shapes["hidden"], shapes["inter"]
+    b = 0
+    for inp, out in ((h, i), (h, i), (i, h)):
+        b += 2 * out * inp + 4 * out + 2 * r * (inp + out)
+    return b + 2 * T * 2 * h
+
+
+def layer_flops(shapes, T, r):
+    return sum(2 * T * (out * inp + r * (inp + out)) for inp, out in proj_list(shapes))
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class Clocks:
+    """nvidia-smi sampling during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.f = None
+
+    def start(self):
+        try:
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = [ln.split(",") for ln in self.f.read().strip().splitlines() if ln.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+                for n, v in zip(names, r[5:9]):
+                    if v.strip().lower().startswith("active"):
+                        reasons.add(n)
+            except (ValueError, IndexError):
+                pass
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- reference
+def run_reference(args):
+    """The fp64 CPU oracle on the host cores, as it stands, on a bounded
+    sample of the same workload (whole layers of the stack at T = 1)."""
+    import oracle
+    import wl_synth
+
+    oracle.build()
+    r = args.rank
+    cores = oracle.get_threads()
+    dims = proj_list(SHAPES)
+    g = wl_synth.make_generator(0)
+    x = wl_synth.draw_x(g, 1, SHAPES["hidden"])
+    thetas = [wl_synth.draw_theta(g, inp, out, r) for inp, out in dims]
+
+    def one_layer(xin):
+        q = oracle.linear(xin, thetas[0])
+        oracle.linear(xin, thetas[1])
+        oracle.linear(xin, thetas[2])
+        import torch
+        qb = torch.from_numpy(q).to(torch.bfloat16)
+        o = oracle.linear(qb, thetas[3])
+        ob = torch.from_numpy(o).to(torch.bfloat16)
+        y = oracle.mlp_geglu(ob, thetas[4], thetas[5], thetas[6])
+        return torch.from_numpy(y).to(torch.bfloat16)
+
+    for _ in range(args.warmup):
+        one_layer(x)
+    times = []
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        one_layer(x)
+        times.append(time.perf_counter() - t0)
+    wall = time.perf_counter() - t_all
+    lb = layer_bytes(SHAPES, 1, r)
+    per_layer = sum(times) / len(times)
+    value = lb / per_layer / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(per_layer * L_LAYERS * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"gemma3-1b decode layer stack, T=1, r={r}, bf16 inputs, "
+                               f"{L_LAYERS} layers (one layer per timed sample)",
+                   "L2": "n/a (CPU)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                         "kind": "oracle",
+                         "sample": f"{args.steps} single layers (1 of {L_LAYERS}) of the stack at T=1; "
+                                   f"ms_per_step extrapolated x{L_LAYERS}; wall {wall:.1f}s"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def time_oracle_sample(r, budget_s=12.0):
+    """cpu_baseline of the wl arm: oracle on a bounded sample (whole layers)."""
+    import oracle
+    import torch
+    import wl_synth
+
+    oracle.build()
+    dims = proj_list(SHAPES)
+    g = wl_synth.make_generator(1)
+    x = wl_synth.draw_x(g, 1, SHAPES["hidden"])
+    thetas = [wl_synth.draw_theta(g, inp, out, r) for inp, out in dims]
+    n = 0
+    t0 = time.perf_counter()
+    while True:
+        q = oracle.linear(x, thetas[0])
+        oracle.linear(x, thetas[1])
+        oracle.linear(x, thetas[2])
+        o = oracle.linear(torch.from_numpy(q).to(torch.bfloat16), thetas[3])
+        oracle.mlp_geglu(torch.from_numpy(o).to(torch.bfloat16), *thetas[4:])
+        n += 1
+        el = time.perf_counter() - t0
+        if el > budget_s or n >= 50:
+            break
+    value = layer_bytes(SHAPES, 1, r) * n / el / 1e9
+    return {"value": round(value, 4), "unit": "GB/s", "cores": oracle.get_threads(),
+            "kind": "oracle", "sample": f"{n} layers of the T=1 stack (of {L_LAYERS}), {el:.1f}s"}
+
+
+# ---------------------------------------------------------------- wl arm --
+def run_wl(args):
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import rank_weight_reconstruction_wl_gb300 as wl
+    from rank_weight_reconstruction_wl_gb300.stack import DecoderStack, build_layers
+
+    r = args.rank
+    T = 1
+    layers = build_layers(L_LAYERS, L_LAYERS, T, SHAPES, r, seed=rank, device=dev)
+    stack = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev)
+    gx = torch.Generator(device=dev)
+    gx.manual_seed(100 + rank)
+    stack.x.copy_(torch.randn(T, SHAPES["hidden"], generator=gx, device=dev).to(torch.bfloat16))
+    stack.capture()
+
+    def barrier():
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            dist.barrier()
+
+    # ---- device-timed steps (graph replay) ----
+    for _ in range(args.warmup):
+        stack.step()
+    barrier()
+    clocks = Clocks(local)
+    clocks.start()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stack.stream)
+    for _ in range(args.steps):
+        stack.step()
+    ev1.record(stack.stream)
+    barrier()
+    ck = clocks.stop()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    step_bytes = layer_bytes(SHAPES, T, r) * L_LAYERS
+    value = step_bytes * world / (ms * 1e-3) / 1e9
+    status = wl.wl_device_status(stack.stream)
+
+    # ---- dominant kernel: the fused MLP, per-launch events on its stream ----
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(L_LAYERS)]
+    mlp_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        stack.step(mlp_events=evs)
+        stack.stream.synchronize()
+        mlp_ms.extend(a.elapsed_time(b) for a, b in evs)
+    mlp_ms_avg = statistics.mean(mlp_ms)
+    hbm_peak, _, peak_kind = load_peaks()
+    mb = mlp_bytes(SHAPES, T, r)
+    achieved = mb / (mlp_ms_avg * 1e-3) / 1e9
+    traffic = load_traffic()
+
+    # ---- end to end through the public API with pinned host buffers ----
+    xh = torch.empty(T, SHAPES["hidden"], dtype=torch.bfloat16).pin_memory()
+    yh = torch.empty(T, SHAPES["hidden"], dtype=torch.bfloat16).pin_memory()
+    xh.copy_(stack.x.cpu())
+    for _ in range(args.warmup):
+        stack.forward_host(xh, yh)
+    barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stack.stream)
+    for _ in range(args.steps):
+        stack.forward_host(xh, yh)
+    t1.record(stack.stream)
+    barrier()
+    e2e_ms = t0.elapsed_time(t1) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"gemma3-1b decode layer stack: {L_LAYERS} layers x (fused QKV "
+                                   f"1152->1024/256/256, O 1024->1152, fused GeGLU MLP 1152->6912->1152), "
+                                   f"T=1, r={r}, G={L_LAYERS} (one W0 per layer)",
+                       "T": T, "r": r, "layers": L_LAYERS,
+                       "l2": "inputs larger than L2 (1.4 GB of distinct weights per step), no flush",
+                       "parallelism": f"replicas x{world}",
+                       "step_bytes": step_bytes,
+                       "us_per_token_per_layer": round(ms * 1e3 / (T * L_LAYERS), 3),
+                       "us_per_token_per_stack": round(ms * 1e3 / T, 2),
+                       "graph": "CUDA graph replay of the stack"},
+            "roofline": {"bound": "hbm", "kernel": "dec_mlp_kernel (fused GeGLU MLP, T=1)",
+                         "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                         "bytes_per_launch": mb, "avg_launch_us": round(mlp_ms_avg * 1e3, 3),
+                         "traffic": traffic},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                    "h2d_bytes_per_step": T * SHAPES["hidden"] * 2,
+                    "d2h_bytes_per_step": T * SHAPES["hidden"] * 2,
+                    "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": stack.launches_per_step * args.steps,
+            "device_status": wl.STATUS_NAMES.get(status, status),
+        }
+        if ck is not None:
+            line["clocks"] = ck
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = time_oracle_sample(r)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def load_traffic():
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary (null if none was taken for the current kernel)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d.get("dec_mlp_kernel")
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="wl", choices=["wl", "reference"])
+    ap.add_argument("--rank", type=int, default=4, help="LoRA rank r of the theta bundles")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        if int(os.environ.get("RANK", "0")) != 0:
+            return
+        if args.steps > 20:
+            args.steps = 20
+        run_reference(args)
+        return
+    run_wl(args)
+
+
+if __name__ == "__main__":
+    main()

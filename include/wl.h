@@ -1,0 +1,160 @@
+/*
+ * wl.h -- C ABI of libwl.so, weightless linear projections on GB300 (sm_103a).
+ *
+ * A weightless projection never holds its dense weight.  Each weight is the
+ * theta bundle of the "Serve and generate with weightless" page (overview):
+ * a W0 block shared per band of layers, a per-output-row scale s and a rank-r
+ * delta U, V.  Every call rebuilds the projection inside the kernel
+ * ("In-kernel reconstruction" page, formula section):
+ *
+ *     y[t,o] = s[o] * sum_i W0[o,i] x[t,i] + sum_k U[o,k] * sum_i V[i,k] x[t,i]
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  Layouts (row-major, contiguous, PyTorch Linear convention):
+ *    x  [T, in]   bf16          W0 [out, in] bf16        s [out] fp32
+ *    U  [out, r]  bf16          V  [in, r]   bf16        y [T, out] bf16 or fp32
+ *  Precision: bf16 inputs, fp32 accumulation, fp32 combine, one final
+ *    round-to-nearest-even cast to the output type ("In-kernel
+ *    reconstruction": the custom-op path accumulates in float32; the GEMM
+ *    path does its final combine in float32 before the cast).
+ *  Memory: every pointer is device memory owned by the caller.  The library
+ *    allocates nothing in these calls.  Outputs must not alias inputs.
+ *  Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Calls
+ *    are asynchronous on that stream; results are ready when it is.
+ *  Errors: return codes only; nothing is thrown or aborted across the ABI.
+ *    Arguments are checked before anything is launched; on error nothing is
+ *    launched and wl_last_error() describes the failure.  A failed launch
+ *    returns WL_ERR_CUDA.  Kernel-side bounded waits that give up record
+ *    WL_ERR_TIMEOUT in a device status word, read by wl_device_status().
+ *  Limits: T >= 1, in >= 8, out >= 1, in % 8 == 0, 0 <= r <= WL_MAX_RANK;
+ *    x, W0 and y must be 16-byte aligned (in % 8 == 0 keeps every row of x
+ *    and W0 aligned when the base is); U and V may be NULL only if r == 0.
+ */
+#ifndef WL_H_
+#define WL_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WL_OK = 0,
+    WL_ERR_INVALID_ARG = 1, /* bad pointer, size, alignment or rank        */
+    WL_ERR_UNSUPPORTED = 2, /* valid arguments this build cannot run       */
+    WL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed        */
+    WL_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up          */
+    WL_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small  */
+} wl_status;
+
+typedef enum { WL_OUT_BF16 = 0, WL_OUT_F32 = 1 } wl_out_dtype;
+
+/* One projection's theta bundle: W0 [out, in], s [out], U [out, r], V [in, r]. */
+typedef struct {
+    const void *W0;
+    const float *s;
+    const void *U;
+    const void *V;
+    int64_t out;
+} wl_proj;
+
+#define WL_MAX_RANK 128
+
+/*
+ * wl_linear -- one weightless projection, y = s*(x W0^T) + (x V) U^T.
+ * Source: "In-kernel reconstruction", formula section (per-element form) and
+ * "The GEMM path" (the same map as s[None,:]*(x@W0.T) + (x@V)@U.T).
+ * x [T,in] bf16, W0 [out,in] bf16, s [out] fp32, U [out,r] bf16, V [in,r] bf16,
+ * y [T,out] of type ydt.  Small T (decode) streams W0 once from HBM with the
+ * rank-r term and the scale folded into the same launch; large T (prefill)
+ * runs the dense contraction on the tensor cores with the low-rank term in
+ * the epilogue.  Both give the same result within fp32 accumulation order.
+ */
+wl_status wl_linear(const void *x, const void *W0, const float *s, const void *U,
+                    const void *V, void *y, int64_t T, int64_t in, int64_t out,
+                    int64_t r, wl_out_dtype ydt, void *stream);
+
+/*
+ * wl_qkv_fused -- the three attention projections that share one input x, in
+ * one launch that reads x once ("In-kernel reconstruction", "Q/K/V fusion").
+ * Each of q, k, v is a full theta bundle with its own out (in and r shared);
+ * yq [T,q.out], yk [T,k.out], yv [T,v.out].  Equal, within accumulation
+ * order, to three wl_linear calls.
+ */
+wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
+                       void *yk, void *yv, int64_t T, int64_t in, int64_t r,
+                       wl_out_dtype ydt, void *stream);
+
+/*
+ * wl_mlp_workspace_bytes -- bytes of device workspace wl_mlp_geglu_fused
+ * needs for these sizes (the intermediate h = gelu(g)*u, the low-rank
+ * partials of the down projection and a grid-barrier word pair).
+ * Returns 0 for invalid sizes.
+ */
+size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t r,
+                              wl_out_dtype ydt);
+
+/*
+ * wl_mlp_geglu_fused -- the gated MLP of a weightless layer in one call
+ * ("In-kernel reconstruction", custom-op path: gate, up, activation and down
+ * fused into one dispatch):
+ *     g = wl(x; gate), u = wl(x; up)          [T, inter]
+ *     h = gelu_tanh(g) * u                    [T, inter]
+ *     y = wl(h; down)                         [T, hidden]   (down.out == hidden)
+ * gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).
+ * workspace: caller-owned device memory of at least
+ * wl_mlp_workspace_bytes(T, hidden, inter, r, ydt) bytes, 256-byte aligned,
+ * ZEROED ONCE before its first use; every call leaves its barrier words at
+ * zero for the next call.  After wl_device_status() reports WL_ERR_TIMEOUT the
+ * workspace must be zeroed again.  Calls sharing one workspace must not
+ * overlap in time.
+ */
+wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj down,
+                             void *y, int64_t T, int64_t hidden, int64_t inter,
+                             int64_t r, void *workspace, size_t ws_bytes,
+                             wl_out_dtype ydt, void *stream);
+
+/*
+ * wl_materialize -- W_eff = s*W0 + U V^T, formed once (the load-time
+ * precompute of "Serve and generate with weightless", "Set the fast path on
+ * NVIDIA").  W_eff [out, in] of type dt (fp32 or bf16).  Bit-exact with one
+ * fixed fp32 order per element:
+ *     d = +0; for k = 0..r-1: d = fma(U[o,k], V[i,k], d)
+ *     w = fl(s[o] * W0[o,i]); if r > 0: w = fl(w + d)
+ * then, for bf16, one round-to-nearest-even.
+ */
+wl_status wl_materialize(const void *W0, const float *s, const void *U, const void *V,
+                         void *W_eff, int64_t out, int64_t in, int64_t r,
+                         wl_out_dtype dt, void *stream);
+
+/*
+ * wl_band_of_layer -- which of the G shared W0 blocks layer `layer` of an
+ * L-layer stack uses: floor(layer * G / L) (contiguous bands).  G = L is the
+ * passthrough point (one W0 per layer, "Set the fast path on NVIDIA"); G = 1
+ * shares one block ("What weightless inference costs", Compression).
+ * Returns -1 unless 0 <= layer < L and 1 <= G <= L.  Host-only, exact.
+ */
+int64_t wl_band_of_layer(int64_t layer, int64_t L, int64_t G);
+
+/*
+ * wl_device_status -- synchronise `stream`, then read and clear the device
+ * status word of the current device.  Returns WL_ERR_TIMEOUT if a bounded
+ * wait in a kernel of this library gave up since the last read, WL_ERR_CUDA
+ * if the synchronisation failed, else WL_OK.
+ */
+wl_status wl_device_status(void *stream);
+
+/* Message for the last error on the calling thread ("" if none). */
+const char *wl_last_error(void);
+
+/* Library version string. */
+const char *wl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WL_H_ */

@@ -1,0 +1,277 @@
+"""Weightless linear projections on GB300: thin Python binding of libwl.so.
+
+Every function here marshals torch CUDA tensors into the C ABI declared in
+``include/wl.h`` and calls it; all arithmetic runs in the library's CUDA
+kernels.  There is no Python or CPU fallback: if ``libwl.so`` is missing or a
+call fails, an exception is raised.
+
+The weightless projection ("In-kernel reconstruction", formula section):
+
+    y[t,o] = s[o] * sum_i W0[o,i] x[t,i] + sum_k U[o,k] * sum_i V[i,k] x[t,i]
+
+Theta arguments (``q``, ``gate`` ...) are any object with ``W0, s, U, V``
+attributes, or a ``(W0, s, U, V)`` tuple.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+import torch
+
+__all__ = [
+    "WLError", "lib", "library_path", "wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes",
+    "wl_mlp_geglu_fused", "wl_materialize", "wl_band_of_layer", "wl_device_status",
+    "wl_last_error", "wl_version", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
+    "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libwl.so")
+
+WL_OK, WL_ERR_INVALID_ARG, WL_ERR_UNSUPPORTED, WL_ERR_CUDA, WL_ERR_TIMEOUT, WL_ERR_WORKSPACE = range(6)
+WL_OUT_BF16, WL_OUT_F32 = 0, 1
+WL_MAX_RANK = 128
+STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3: "WL_ERR_CUDA",
+                4: "WL_ERR_TIMEOUT", 5: "WL_ERR_WORKSPACE"}
+
+# Every function include/wl.h declares.
+EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
+                    "wl_materialize", "wl_band_of_layer", "wl_device_status", "wl_last_error",
+                    "wl_version")
+
+
+class WLError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+class _Proj(C.Structure):
+    _fields_ = [("W0", C.c_void_p), ("s", C.c_void_p), ("U", C.c_void_p), ("V", C.c_void_p),
+                ("out", C.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def lib():
+    """Load libwl.so (built in-tree by build.py); raise if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise RuntimeError(
+                f"libwl.so not found at {_LIB_PATH}; build it with "
+                "`python -m rank_weight_reconstruction_wl_gb300.build` (needs nvcc)")
+        L = C.CDLL(_LIB_PATH)
+        i64, vp, st = C.c_int64, C.c_void_p, C.c_int
+        L.wl_linear.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, C.c_int, vp]
+        L.wl_linear.restype = st
+        L.wl_qkv_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, vp, vp, i64, i64, i64, C.c_int, vp]
+        L.wl_qkv_fused.restype = st
+        L.wl_mlp_workspace_bytes.argtypes = [i64, i64, i64, i64, C.c_int]
+        L.wl_mlp_workspace_bytes.restype = C.c_size_t
+        L.wl_mlp_geglu_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, i64, i64, i64, i64, vp,
+                                         C.c_size_t, C.c_int, vp]
+        L.wl_mlp_geglu_fused.restype = st
+        L.wl_materialize.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, C.c_int, vp]
+        L.wl_materialize.restype = st
+        L.wl_band_of_layer.argtypes = [i64, i64, i64]
+        L.wl_band_of_layer.restype = i64
+        L.wl_device_status.argtypes = [vp]
+        L.wl_device_status.restype = st
+        L.wl_last_error.restype = C.c_char_p
+        L.wl_version.restype = C.c_char_p
+        _lib = L
+        return L
+
+
+# ------------------------------------------------------------ marshalling --
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _theta(th):
+    if isinstance(th, (tuple, list)):
+        return tuple(th)
+    return th.W0, th.s, th.U, th.V
+
+
+def _proj(th, inp: int, r: int, name: str):
+    W0, s, U, V = _theta(th)
+    out = W0.shape[0]
+    _need(W0, f"{name}.W0", torch.bfloat16, (out, inp))
+    _need(s, f"{name}.s", torch.float32, (out,))
+    if r > 0:
+        _need(U, f"{name}.U", torch.bfloat16, (out, r))
+        _need(V, f"{name}.V", torch.bfloat16, (inp, r))
+    return _Proj(W0.data_ptr(), s.data_ptr(), U.data_ptr() if r > 0 else None,
+                 V.data_ptr() if r > 0 else None, out)
+
+
+def _rank(th) -> int:
+    U = _theta(th)[2]
+    return 0 if U is None else int(U.shape[1])
+
+
+def _ydt(dtype) -> int:
+    if dtype in (torch.bfloat16, "bf16"):
+        return WL_OUT_BF16
+    if dtype in (torch.float32, "f32", "fp32"):
+        return WL_OUT_F32
+    raise ValueError(f"output dtype must be bfloat16 or float32, got {dtype}")
+
+
+def _tdt(ydt: int):
+    return torch.float32 if ydt == WL_OUT_F32 else torch.bfloat16
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    if isinstance(stream, torch.cuda.Stream):
+        return C.c_void_p(stream.cuda_stream)
+    return C.c_void_p(int(stream))
+
+
+def _check(status: int):
+    if status != WL_OK:
+        raise WLError(status, lib().wl_last_error().decode())
+
+
+# -------------------------------------------------------------------- API --
+def wl_linear(x, W0, s, U, V, y=None, ydt=torch.bfloat16, stream=None):
+    """y = s*(x W0^T) + (x V) U^T  (x [T,in] bf16 -> y [T,out] bf16/fp32)."""
+    T, inp = x.shape
+    out = W0.shape[0]
+    r = 0 if U is None else int(U.shape[1])
+    code = _ydt(ydt)
+    _need(x, "x", torch.bfloat16)
+    p = _proj((W0, s, U, V), inp, r, "theta")
+    if y is None:
+        y = torch.empty(T, out, dtype=_tdt(code), device=x.device)
+    _need(y, "y", _tdt(code), (T, out))
+    with torch.cuda.device(x.device):
+        _check(lib().wl_linear(_ptr(x), p.W0, p.s, p.U, p.V, _ptr(y), T, inp, out, r, code,
+                               _stream(stream, x.device)))
+    return y
+
+
+def wl_qkv_fused(x, q, k, v, outs=None, ydt=torch.bfloat16, stream=None):
+    """Q/K/V projections of one x in one launch; returns (yq, yk, yv)."""
+    T, inp = x.shape
+    r = _rank(q)
+    code = _ydt(ydt)
+    _need(x, "x", torch.bfloat16)
+    ps = [_proj(th, inp, r, n) for th, n in ((q, "q"), (k, "k"), (v, "v"))]
+    if outs is None:
+        outs = tuple(torch.empty(T, p.out, dtype=_tdt(code), device=x.device) for p in ps)
+    for o, p, n in zip(outs, ps, ("yq", "yk", "yv")):
+        _need(o, n, _tdt(code), (T, p.out))
+    with torch.cuda.device(x.device):
+        _check(lib().wl_qkv_fused(_ptr(x), ps[0], ps[1], ps[2], _ptr(outs[0]), _ptr(outs[1]),
+                                  _ptr(outs[2]), T, inp, r, code, _stream(stream, x.device)))
+    return tuple(outs)
+
+
+def wl_mlp_workspace_bytes(T, hidden, inter, r, ydt=torch.bfloat16) -> int:
+    return int(lib().wl_mlp_workspace_bytes(T, hidden, inter, r, _ydt(ydt)))
+
+
+_ws_cache: dict = {}
+
+
+def mlp_workspace(T, hidden, inter, r, ydt=torch.bfloat16, device=None) -> torch.Tensor:
+    """A zeroed workspace of the right size (cached per device and size)."""
+    n = wl_mlp_workspace_bytes(T, hidden, inter, r, ydt)
+    if n == 0:
+        raise ValueError("invalid MLP sizes")
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    key = (dev.index, n)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        ws = torch.zeros(n + 256, dtype=torch.uint8, device=dev)
+        off = (-ws.data_ptr()) % 256
+        ws = ws[off:off + n]
+        _ws_cache[key] = ws
+    return ws
+
+
+def wl_mlp_geglu_fused(x, gate, up, down, y=None, workspace=None, ydt=torch.bfloat16,
+                       stream=None):
+    """y = (gelu_tanh(x Wg^T) * (x Wu^T)) Wd^T with every W a weightless projection."""
+    T, hidden = x.shape
+    r = _rank(gate)
+    inter = _theta(gate)[0].shape[0]
+    code = _ydt(ydt)
+    _need(x, "x", torch.bfloat16)
+    pg = _proj(gate, hidden, r, "gate")
+    pu = _proj(up, hidden, r, "up")
+    pd = _proj(down, inter, r, "down")
+    if y is None:
+        y = torch.empty(T, hidden, dtype=_tdt(code), device=x.device)
+    _need(y, "y", _tdt(code), (T, hidden))
+    if workspace is None:
+        workspace = mlp_workspace(T, hidden, inter, r, ydt, x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().wl_mlp_geglu_fused(_ptr(x), pg, pu, pd, _ptr(y), T, hidden, inter, r,
+                                        _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                        code, _stream(stream, x.device)))
+    return y
+
+
+def wl_materialize(W0, s, U, V, dt=torch.bfloat16, out=None, stream=None):
+    """W_eff = s*W0 + U V^T, bit-exact fixed fp32 order, as bf16 or fp32."""
+    o, inp = W0.shape
+    r = 0 if U is None else int(U.shape[1])
+    code = _ydt(dt)
+    p = _proj((W0, s, U, V), inp, r, "theta")
+    if out is None:
+        out = torch.empty(o, inp, dtype=_tdt(code), device=W0.device)
+    _need(out, "W_eff", _tdt(code), (o, inp))
+    with torch.cuda.device(W0.device):
+        _check(lib().wl_materialize(p.W0, p.s, p.U, p.V, _ptr(out), o, inp, r, code,
+                                    _stream(stream, W0.device)))
+    return out
+
+
+def wl_band_of_layer(layer: int, L: int, G: int) -> int:
+    return int(lib().wl_band_of_layer(layer, L, G))
+
+
+def wl_device_status(stream=None, device=None) -> int:
+    """Synchronise and return (and clear) the device status code."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        return int(lib().wl_device_status(_stream(stream, dev)))
+
+
+def wl_last_error() -> str:
+    return lib().wl_last_error().decode()
+
+
+def wl_version() -> str:
+    return lib().wl_version().decode()

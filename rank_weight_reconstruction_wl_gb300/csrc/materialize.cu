@@ -1,0 +1,124 @@
+// materialize.cu -- W_eff = s*W0 + U V^T, formed once ("Serve and generate
+// with weightless", "Set the fast path on NVIDIA": the effective weight is
+// materialised at load time and every projection becomes one dense matmul).
+//
+// Bit-exact contract, per element (the pages give no order; this one is the
+// library's):
+//     d = +0; for k = 0..r-1 ascending: d = fma(U[o,k], V[i,k], d)
+//     w = fl(s[o] * W0[o,i]); if r > 0: w = fl(w + d)
+// and, for a bf16 result, one round-to-nearest-even.  The tensor cores are
+// not used: their accumulation order is not this one.
+//
+// Tiling: a CTA owns a 64 x 256 tile of W_eff (8 rows x 8 columns per
+// thread).  U and V are staged through shared memory in chunks of 32 ranks
+// (transposed, so each k step reads one float4 pair of V and of U), which
+// keeps the rank-r operands out of HBM after their first read: V is re-read
+// once per 64 output rows, U once per 256 input columns, both from L2.
+#include "wl_internal.cuh"
+
+namespace wl {
+
+constexpr int kMatRows = 64;
+constexpr int kMatCols = 256;
+constexpr int kMatK = 32;
+constexpr int kUStr = kMatRows + 4;  // padded row strides (floats), multiples of 4
+constexpr int kVStr = kMatCols + 4;
+
+template <int F32OUT>
+__global__ void __launch_bounds__(kThreads) materialize_kernel(
+    const bf16 *__restrict__ W0, const float *__restrict__ s, const bf16 *__restrict__ U,
+    const bf16 *__restrict__ V, void *__restrict__ Weff, int out, int in, int r)
+{
+    __shared__ __align__(16) float Us[kMatK * kUStr];
+    __shared__ __align__(16) float Vs[kMatK * kVStr];
+    const int o_base = blockIdx.y * kMatRows;
+    const int i_base = blockIdx.x * kMatCols;
+    const int tr = threadIdx.x >> 5;  // rows o_base + tr*8 .. +7
+    const int tc = threadIdx.x & 31;  // cols i_base + tc*8 .. +7
+
+    float d[8][8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) d[a][b] = 0.0f;
+
+    for (int k0 = 0; k0 < r; k0 += kMatK) {
+        const int kn = min(kMatK, r - k0);
+        for (int idx = threadIdx.x; idx < kMatRows * kMatK; idx += kThreads) {
+            const int o = idx / kMatK, k = idx - o * kMatK;
+            float v = 0.f;
+            if (k < kn && o_base + o < out) v = bf2f(U[(int64_t)(o_base + o) * r + k0 + k]);
+            Us[k * kUStr + o] = v;
+        }
+        for (int idx = threadIdx.x; idx < kMatCols * kMatK; idx += kThreads) {
+            const int i = idx / kMatK, k = idx - i * kMatK;
+            float v = 0.f;
+            if (k < kn && i_base + i < in) v = bf2f(V[(int64_t)(i_base + i) * r + k0 + k]);
+            Vs[k * kVStr + i] = v;
+        }
+        __syncthreads();
+        for (int k = 0; k < kn; ++k) {
+            const float4 u0 = *reinterpret_cast<const float4 *>(Us + k * kUStr + tr * 8);
+            const float4 u1 = *reinterpret_cast<const float4 *>(Us + k * kUStr + tr * 8 + 4);
+            const float4 v0 = *reinterpret_cast<const float4 *>(Vs + k * kVStr + tc * 8);
+            const float4 v1 = *reinterpret_cast<const float4 *>(Vs + k * kVStr + tc * 8 + 4);
+            const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+            for (int a = 0; a < 8; ++a)
+#pragma unroll
+                for (int b = 0; b < 8; ++b) d[a][b] = __fmaf_rn(uu[a], vv[b], d[a][b]);
+        }
+        __syncthreads();
+    }
+
+    const int i0 = i_base + tc * 8;
+    if (i0 >= in) return;  // in % 8 == 0: a chunk of 8 columns is all in or all out
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int o = o_base + tr * 8 + a;
+        if (o >= out) break;
+        const float sv = s[o];
+        const uint4 wv = *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0);
+        const float w0[8] = {bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y),
+                             bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w)};
+        float w[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            w[b] = __fmul_rn(sv, w0[b]);
+            if (r > 0) w[b] = __fadd_rn(w[b], d[a][b]);
+        }
+        if (F32OUT) {
+            float *dst = static_cast<float *>(Weff) + (int64_t)o * in + i0;
+            reinterpret_cast<float4 *>(dst)[0] = make_float4(w[0], w[1], w[2], w[3]);
+            reinterpret_cast<float4 *>(dst)[1] = make_float4(w[4], w[5], w[6], w[7]);
+        } else {
+            uint32_t p[4];
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                const __nv_bfloat162 h2 = __floats2bfloat162_rn(w[2 * b], w[2 * b + 1]);
+                p[b] = *reinterpret_cast<const uint32_t *>(&h2);
+            }
+            bf16 *dst = static_cast<bf16 *>(Weff) + (int64_t)o * in + i0;
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+    }
+}
+
+wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U, const bf16 *V,
+                             void *W_eff, int64_t out, int64_t in, int64_t r, int dt,
+                             cudaStream_t st)
+{
+    const dim3 grid((unsigned)((in + kMatCols - 1) / kMatCols),
+                    (unsigned)((out + kMatRows - 1) / kMatRows));
+    if (grid.y > 65535u) return fail(WL_ERR_UNSUPPORTED, "materialize: out too large (%lld)", (long long)out);
+    if (dt == WL_OUT_F32)
+        materialize_kernel<1><<<grid, kThreads, 0, st>>>(W0, s, U, V, W_eff, (int)out, (int)in, (int)r);
+    else
+        materialize_kernel<0><<<grid, kThreads, 0, st>>>(W0, s, U, V, W_eff, (int)out, (int)in, (int)r);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "materialize launch");
+    return WL_OK;
+}
+
+}  // namespace wl

@@ -1,0 +1,90 @@
+// wl_internal.cuh -- device helpers and host launch declarations shared by
+// the translation units of libwl.so.  Nothing here is part of the C ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "wl.h"
+
+namespace wl {
+
+typedef __nv_bfloat16 bf16;
+
+constexpr int kThreads = 256;  // CTA size of the decode and materialize kernels
+constexpr int kWarps = kThreads / 32;
+
+// Largest token count the CUDA-core decode kernels hold per pass.
+constexpr int kDecodeTT = 8;
+
+// ---------------------------------------------------------------- device --
+// bf16 pair packed in a 32-bit word -> two fp32 values (exact).  The element
+// at the lower address sits in the low half of the word.
+__device__ __forceinline__ float bf_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t u) { return __uint_as_float(u & 0xffff0000u); }
+__device__ __forceinline__ float bf2f(bf16 v) { return __bfloat162float(v); }
+
+// 16-byte streaming load: read-only path, no L1 allocation (the data is used
+// once; L2 still sees it).
+__device__ __forceinline__ uint4 ld_stream16(const void *p)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Device status bits (OR-ed into the library's status word).
+constexpr unsigned kStatusTimeout = 1u;
+
+// Upper bound of every spin-wait in this library.  A wait that runs longer
+// sets kStatusTimeout and returns instead of waiting further.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ void store_out(void *y, int ydt, int64_t idx, float v)
+{
+    if (ydt == WL_OUT_F32)
+        static_cast<float *>(y)[idx] = v;
+    else
+        static_cast<bf16 *>(y)[idx] = __float2bfloat16_rn(v);
+}
+
+// ------------------------------------------------------------------ host --
+struct DeviceInfo {
+    int device;
+    int sm_count;
+    int max_smem_optin;
+    int l2_bytes;
+    unsigned *status;  // device address of this library's status word
+};
+
+// Per-device facts of the current device, queried once per device.
+const DeviceInfo *device_info(wl_status *st);
+
+// Record a message for wl_last_error() and return the status.
+wl_status fail(wl_status st, const char *fmt, ...);
+wl_status cuda_fail(cudaError_t e, const char *what);
+
+// Kernel launchers (arguments already validated by the C-ABI layer).
+wl_status launch_decode_linear(const bf16 *x, const wl_proj *proj, int nproj,
+                               void *const *y, int64_t T, int64_t in, int64_t r,
+                               int ydt, cudaStream_t st);
+wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up,
+                            const wl_proj &down, void *y, int64_t T, int64_t hidden,
+                            int64_t inter, int64_t r, void *ws, size_t ws_bytes,
+                            int ydt, cudaStream_t st);
+size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r);
+wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U,
+                             const bf16 *V, void *W_eff, int64_t out, int64_t in,
+                             int64_t r, int dt, cudaStream_t st);
+
+}  // namespace wl

@@ -18,3 +18,24 @@ def orc():
 
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def wl():
+    """The CUDA library's Python binding (built in-tree if stale)."""
+    from rank_weight_reconstruction_wl_gb300 import build
+
+    build.build()
+    import rank_weight_reconstruction_wl_gb300 as pkg
+
+    pkg.lib()
+    return pkg
+
+
+@pytest.fixture(scope="session")
+def gpu():
+    import torch
+
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    return torch.device("cuda", 0)
