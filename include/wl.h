@@ -118,6 +118,28 @@ wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj do
                              wl_out_dtype ydt, void *stream);
 
 /*
+ * wl_mlp_geglu_fused_noalloc -- the same fused GeGLU MLP as
+ * wl_mlp_geglu_fused, for callers that cannot allocate device memory (code
+ * that may not call cudaMalloc, such as a host callback, an allocator hook or
+ * a process whose device-memory budget is fixed at start-up).  It takes no
+ * workspace: it uses a 4 MiB scratch array built into libwl.so, which every
+ * GPU that loads the library holds until the process exits.  The documentation
+ * pages have no counterpart to this call; it exists for such callers.
+ *   - Sizes whose workspace (wl_mlp_workspace_bytes) exceeds 4 MiB are
+ *     rejected with WL_ERR_UNSUPPORTED and a message; nothing is launched.
+ *   - The first call on a device looks up the scratch address for that device
+ *     (make it before any stream capture on that device).
+ *   - Every call clears the scratch's barrier words on `stream`, then runs the
+ *     MLP; no call allocates or frees memory.
+ *   - All calls share the one scratch array: calls that overlap on the GPU
+ *     (different streams, or different host threads) race and give wrong
+ *     results.  Serialise them.
+ */
+wl_status wl_mlp_geglu_fused_noalloc(const void *x, wl_proj gate, wl_proj up, wl_proj down,
+                                     void *y, int64_t T, int64_t hidden, int64_t inter,
+                                     int64_t r, wl_out_dtype ydt, void *stream);
+
+/*
  * wl_materialize -- W_eff = s*W0 + U V^T, formed once (the load-time
  * precompute of "Serve and generate with weightless", "Set the fast path on
  * NVIDIA").  W_eff [out, in] of type dt (fp32 or bf16).  Bit-exact with one

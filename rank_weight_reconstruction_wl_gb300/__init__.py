@@ -22,7 +22,7 @@ import torch
 
 __all__ = [
     "WLError", "lib", "library_path", "wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes",
-    "wl_mlp_geglu_fused", "wl_materialize", "wl_band_of_layer", "wl_device_status",
+    "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status",
     "wl_last_error", "wl_version", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
     "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
 ]
@@ -38,7 +38,7 @@ STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3:
 
 # Every function include/wl.h declares.
 EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
-                    "wl_materialize", "wl_band_of_layer", "wl_device_status", "wl_last_error",
+                    "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status", "wl_last_error",
                     "wl_version")
 
 
@@ -82,6 +82,9 @@ def lib():
         L.wl_mlp_geglu_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, i64, i64, i64, i64, vp,
                                          C.c_size_t, C.c_int, vp]
         L.wl_mlp_geglu_fused.restype = st
+        L.wl_mlp_geglu_fused_noalloc.argtypes = [vp, _Proj, _Proj, _Proj, vp, i64, i64, i64, i64,
+                                                 C.c_int, vp]
+        L.wl_mlp_geglu_fused_noalloc.restype = st
         L.wl_materialize.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, C.c_int, vp]
         L.wl_materialize.restype = st
         L.wl_band_of_layer.argtypes = [i64, i64, i64]
@@ -240,6 +243,24 @@ def wl_mlp_geglu_fused(x, gate, up, down, y=None, workspace=None, ydt=torch.bflo
         _check(lib().wl_mlp_geglu_fused(_ptr(x), pg, pu, pd, _ptr(y), T, hidden, inter, r,
                                         _ptr(workspace), workspace.numel() * workspace.element_size(),
                                         code, _stream(stream, x.device)))
+    return y
+
+
+def wl_mlp_geglu_fused_noalloc(x, gate, up, down, y, ydt=torch.bfloat16, stream=None):
+    """Same MLP without a caller workspace (library's built-in 4 MiB scratch),
+    for callers that cannot allocate device memory.  `y` must be given."""
+    T, hidden = x.shape
+    r = _rank(gate)
+    inter = _theta(gate)[0].shape[0]
+    code = _ydt(ydt)
+    _need(x, "x", torch.bfloat16)
+    pg = _proj(gate, hidden, r, "gate")
+    pu = _proj(up, hidden, r, "up")
+    pd = _proj(down, inter, r, "down")
+    _need(y, "y", _tdt(code), (T, hidden))
+    with torch.cuda.device(x.device):
+        _check(lib().wl_mlp_geglu_fused_noalloc(_ptr(x), pg, pu, pd, _ptr(y), T, hidden, inter, r,
+                                                code, _stream(stream, x.device)))
     return y
 
 
