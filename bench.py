@@ -222,7 +222,8 @@ def run_wl(args):
 
     r = args.rank
     T = 1
-    layers = build_layers(L_LAYERS, L_LAYERS, T, SHAPES, r, seed=rank, device=dev)
+    nl = args.layers
+    layers = build_layers(nl, nl, T, SHAPES, r, seed=rank, device=dev)
     stack = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev)
     gx = torch.Generator(device=dev)
     gx.manual_seed(100 + rank)
@@ -253,13 +254,13 @@ def run_wl(args):
         t = torch.tensor([ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
-    step_bytes = layer_bytes(SHAPES, T, r) * L_LAYERS
+    step_bytes = layer_bytes(SHAPES, T, r) * nl
     value = step_bytes * world / (ms * 1e-3) / 1e9
     status = wl.wl_device_status(stack.stream)
 
     # ---- dominant kernel: the fused MLP, per-launch events on its stream ----
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(L_LAYERS)]
+           for _ in range(nl)]
     mlp_ms = []
     for _ in range(max(3, min(args.steps, 10))):
         stack.step(mlp_events=evs)
@@ -298,14 +299,14 @@ def run_wl(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": f"gemma3-1b decode layer stack: {L_LAYERS} layers x (fused QKV "
+            "config": {"workload": f"gemma3-1b decode layer stack: {nl} layers x (fused QKV "
                                    f"1152->1024/256/256, O 1024->1152, fused GeGLU MLP 1152->6912->1152), "
-                                   f"T=1, r={r}, G={L_LAYERS} (one W0 per layer)",
-                       "T": T, "r": r, "layers": L_LAYERS,
+                                   f"T=1, r={r}, G={nl} (one W0 per layer)",
+                       "T": T, "r": r, "layers": nl,
                        "l2": "inputs larger than L2 (1.4 GB of distinct weights per step), no flush",
                        "parallelism": f"replicas x{world}",
                        "step_bytes": step_bytes,
-                       "us_per_token_per_layer": round(ms * 1e3 / (T * L_LAYERS), 3),
+                       "us_per_token_per_layer": round(ms * 1e3 / (T * nl), 3),
                        "us_per_token_per_stack": round(ms * 1e3 / T, 2),
                        "graph": "CUDA graph replay of the stack"},
             "roofline": {"bound": "hbm", "kernel": "dec_mlp_kernel (fused GeGLU MLP, T=1)",
@@ -350,6 +351,8 @@ def main():
     ap.add_argument("--impl", default="wl", choices=["wl", "reference"])
     ap.add_argument("--rank", type=int, default=4, help="LoRA rank r of the theta bundles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=L_LAYERS,
+                    help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -90,9 +90,9 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
 
 /*
  * wl_mlp_workspace_bytes -- bytes of device workspace wl_mlp_geglu_fused
- * needs for these sizes (the intermediate h = gelu(g)*u, the low-rank
- * partials of the down projection and a grid-barrier word pair).
- * Returns 0 for invalid sizes.
+ * needs for these sizes (the intermediate h = gelu(g)*u and the partial sums
+ * of the down projection's low-rank input h V_down).  Returns 0 for invalid
+ * sizes.
  */
 size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t r,
                               wl_out_dtype ydt);
@@ -106,11 +106,9 @@ size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t 
  *     y = wl(h; down)                         [T, hidden]   (down.out == hidden)
  * gelu_tanh(v) = 0.5 v (1 + tanh(sqrt(2/pi) (v + 0.044715 v^3))).
  * workspace: caller-owned device memory of at least
- * wl_mlp_workspace_bytes(T, hidden, inter, r, ydt) bytes, 256-byte aligned,
- * ZEROED ONCE before its first use; every call leaves its barrier words at
- * zero for the next call.  After wl_device_status() reports WL_ERR_TIMEOUT the
- * workspace must be zeroed again.  Calls sharing one workspace must not
- * overlap in time.
+ * wl_mlp_workspace_bytes(T, hidden, inter, r, ydt) bytes, 256-byte aligned;
+ * its contents need no initialisation.  Calls sharing one workspace must not
+ * overlap in time (calls on one stream never do).
  */
 wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj down,
                              void *y, int64_t T, int64_t hidden, int64_t inter,
@@ -129,8 +127,8 @@ wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj do
  *     rejected with WL_ERR_UNSUPPORTED and a message; nothing is launched.
  *   - The first call on a device looks up the scratch address for that device
  *     (make it before any stream capture on that device).
- *   - Every call clears the scratch's barrier words on `stream`, then runs the
- *     MLP; no call allocates or frees memory.
+ *   - The scratch keeps whatever the previous call left; nothing in it has to
+ *     start at zero.  No call allocates or frees memory.
  *   - All calls share the one scratch array: calls that overlap on the GPU
  *     (different streams, or different host threads) race and give wrong
  *     results.  Serialise them.

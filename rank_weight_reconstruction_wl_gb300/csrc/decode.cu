@@ -1,31 +1,50 @@
-// decode.cu -- decode-size (small T) weightless projections on CUDA cores.
+// decode.cu -- decode-size (small T) weightless projections.
 //
 // Computes, for each output row o of a projection ("In-kernel
 // reconstruction", formula section):
 //     y[t,o] = s[o] * sum_i W0[o,i] x[t,i] + sum_k U[o,k] z[t,k],
 //     z[t,k] = sum_i V[i,k] x[t,i]
-// in ONE launch per call: W0 is streamed from HBM exactly once with 16-byte
-// loads, z is formed in the same launch, and the scale and the rank-r delta
-// are applied in the epilogue.  At decode sizes the work is bound by the
-// HBM stream of W0 (one multiply-add per two bytes at T = 1), so these
-// kernels use CUDA cores, not the tensor cores.
+// in ONE launch per call: W0 is streamed from HBM exactly once, z is formed in
+// the same launch, and the scale and the rank-r delta are applied in the
+// epilogue.  At decode sizes the cost is the HBM stream of W0.
 //
-// Work split.  A launch covers a set of projections ("segments": one for
-// wl_linear, three for Q/K/V fusion).  Output rows are cut into row blocks;
-// each row block is handled by a thread-block cluster of KS CTAs that split
-// the input dimension K.  Every CTA computes, over its own K range,
+// CTA organisation (288 threads):
+//   warp 8      producer: one thread streams W0 as 64-row x 64-column tiles
+//               (TMA 2D, 128-byte swizzle) into a ring of shared-memory stages
+//               (two tiles = 16 KB per stage), each completed by an mbarrier
+//               transaction count.  It waits only for a free stage, so HBM
+//               stays busy through the consumers' synchronisation points.
+//   warps 0..7  consumers: stage x, form z over their K range, then multiply
+//               each stage on the tensor cores (mma.sync m16n8k16, bf16 in,
+//               fp32 accumulate) with the W0 rows as the M side and the tokens
+//               as the N side (8 columns per n-tile), and run the epilogue.
+//               One tensor-core instruction covers 16 rows x 16 columns of W0,
+//               which keeps the consumers well ahead of the HBM stream.
+//
+// Work split.  Output rows are cut into groups of 64-row tiles; a group is
+// handled by a thread-block cluster of KS CTAs that split the input dimension
+// K.  Every CTA computes over its K range
 //     p[t,o] = s[o] * sum_{i in range} W0[o,i] x[t,i] + sum_k U[o,k] z_range[t,k]
-// (both terms are linear in the K split, so the ranges add up to y), then the
-// cluster adds the KS partials through distributed shared memory in a fixed
-// rank order (deterministic, no global atomics, no scratch memory).
+// (both terms are linear in the split, so the ranges add up to y).  The KS
+// partials are added through distributed shared memory in a fixed rank order
+// (deterministic, no atomics, no scratch memory); readiness is signalled with
+// remote mbarrier arrivals, so the producer warp never joins a cluster barrier.
 //
 // The fused GeGLU MLP ("In-kernel reconstruction", custom-op path: gate, up,
-// activation and down in one dispatch) runs as one persistent launch in two
-// phases separated by a bounded grid barrier: phase 1 produces h = gelu(g)*u
-// and the down projection's low-rank partials z_down = h V_down, phase 2
-// streams W_down.
+// activation and down in one dispatch) is one call made of two launches
+// chained by programmatic dependent launch: the first forms h = gelu(g)*u and
+// partial sums of z_down = h V_down; the second streams W_down from the moment
+// its CTAs are resident and reads h once the first launch has finished.  (A
+// single persistent launch would need every CTA resident at once for a grid
+// barrier; with overlapping launches that is not guaranteed.)  The second
+// launch takes h as a pair of bf16 columns per token (hi and lo parts), so its
+// tensor-core product keeps fp32 accuracy.
+//
+// Launches use programmatic dependent launch: a kernel lets the next one on
+// the stream start once all its CTAs run; the next kernel's producer streams
+// weights at once, and its consumers wait (griddepcontrol.wait) for the
+// previous kernel to finish before reading its input or writing any output.
 #include <cooperative_groups.h>
-#include <stdio.h>
 
 #include <mutex>
 #include <unordered_map>
@@ -36,149 +55,174 @@ namespace cg = cooperative_groups;
 
 namespace wl {
 
+constexpr int kDecThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
+constexpr int kBR = 64;                     // W0 rows per tile
+constexpr int kBK = 64;                     // W0 columns per TMA box (128 bytes)
+constexpr int kBoxBytes = kBR * kBK * 2;    // 8 KB
+constexpr int kStageBytes = 2 * kBoxBytes;  // two boxes (k-tiles) per ring stage
+constexpr int kTokChunk = 8;                // tokens per pass of the rank-r helpers
+
 // ------------------------------------------------------------------------
-// Shared device pieces
+// PTX helpers: mbarrier, TMA, cluster, tensor cores, dependent launch
 // ------------------------------------------------------------------------
-
-// Stage x[t, k0:k0+klen) (bf16, row stride `ld`) into xs[t*Kc + j] as fp32;
-// rows t >= T are zero.  klen % 8 == 0.
-template <int TT>
-__device__ __forceinline__ void stage_x_bf16(const bf16 *__restrict__ x, int64_t ld, int T,
-                                             int k0, int klen, int Kc, float *xs)
+__device__ __forceinline__ uint32_t smem_u32(const void *p)
 {
-    const int nck = klen >> 3;
-    for (int idx = threadIdx.x; idx < TT * nck; idx += kThreads) {
-        const int t = idx / nck, c = idx - t * nck;
-        float4 lo = make_float4(0.f, 0.f, 0.f, 0.f), hi = lo;
-        if (t < T) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(x + t * ld + k0 + 8 * c);
-            lo = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
-            hi = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
-        }
-        *reinterpret_cast<float4 *>(xs + t * Kc + 8 * c) = lo;
-        *reinterpret_cast<float4 *>(xs + t * Kc + 8 * c + 4) = hi;
-    }
+    return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-// Same from an fp32 source written earlier in this launch (L2-coherent loads).
-template <int TT>
-__device__ __forceinline__ void stage_x_f32(const float *x, int64_t ld, int T, int k0, int klen,
-                                            int Kc, float *xs)
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
 {
-    const int nq = klen >> 2;
-    for (int idx = threadIdx.x; idx < TT * nq; idx += kThreads) {
-        const int t = idx / nq, c = idx - t * nq;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (t < T) v = __ldcg(reinterpret_cast<const float4 *>(x + t * ld + k0 + 4 * c));
-        *reinterpret_cast<float4 *>(xs + t * Kc + 4 * c) = v;
-    }
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
 }
 
-// Raw dot products acc[v*TT + t] = sum_{c < nck} W0row(v)[8c..8c+7] . xs[t][8c..]
-// for the virtual rows v in [0, nv).  row_ptr(v) returns the address of the
-// K-range start of virtual row v.  LPR lanes share one row; a warp works on
-// (32/LPR)*RPI rows at a time.
-template <int TT, int LPR, typename RowPtr>
-__device__ __forceinline__ void stream_rows(RowPtr row_ptr, int nv, int nck, const float *xs,
-                                            int Kc, float *acc)
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, unsigned bytes)
 {
-    constexpr int G = 32 / LPR;
-    constexpr int RPI = (TT <= 2) ? 4 : 2;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int gi = lane / LPR, sl = lane % LPR;
-    for (int rb = warp * G * RPI; rb < nv; rb += kWarps * G * RPI) {
-        float a[RPI][TT];
-        const bf16 *wp[RPI];
-        bool ok[RPI];
-#pragma unroll
-        for (int j = 0; j < RPI; ++j) {
-            const int v = rb + gi * RPI + j;
-            ok[j] = v < nv;
-            wp[j] = row_ptr(ok[j] ? v : 0);
-#pragma unroll
-            for (int t = 0; t < TT; ++t) a[j][t] = 0.f;
-        }
-#pragma unroll 2
-        for (int c = sl; c < nck; c += LPR) {
-            uint4 w[RPI];
-#pragma unroll
-            for (int j = 0; j < RPI; ++j)
-                w[j] = ok[j] ? ld_stream16(wp[j] + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                const float4 xa = *reinterpret_cast<const float4 *>(xs + t * Kc + 8 * c);
-                const float4 xb = *reinterpret_cast<const float4 *>(xs + t * Kc + 8 * c + 4);
-#pragma unroll
-                for (int j = 0; j < RPI; ++j) {
-                    float s = a[j][t];
-                    s = fmaf(bf_lo(w[j].x), xa.x, s);
-                    s = fmaf(bf_hi(w[j].x), xa.y, s);
-                    s = fmaf(bf_lo(w[j].y), xa.z, s);
-                    s = fmaf(bf_hi(w[j].y), xa.w, s);
-                    s = fmaf(bf_lo(w[j].z), xb.x, s);
-                    s = fmaf(bf_hi(w[j].z), xb.y, s);
-                    s = fmaf(bf_lo(w[j].w), xb.z, s);
-                    s = fmaf(bf_hi(w[j].w), xb.w, s);
-                    a[j][t] = s;
-                }
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < RPI; ++j)
-#pragma unroll
-            for (int t = 0; t < TT; ++t) {
-                float s = a[j][t];
-#pragma unroll
-                for (int off = LPR / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-                a[j][t] = s;
-            }
-        if (sl == 0) {
-#pragma unroll
-            for (int j = 0; j < RPI; ++j)
-                if (ok[j]) {
-                    const int v = rb + gi * RPI + j;
-#pragma unroll
-                    for (int t = 0; t < TT; ++t) acc[v * TT + t] = a[j][t];
-                }
-        }
-    }
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
 }
 
-// out[t*ostride + k] = sum_{i < n} src[t*sstride + i] * V[i*r + k], k < r.
-// All threads of the CTA take part (contains __syncthreads).  zred holds
-// kWarps*TT*32 floats.
-template <int TT>
-__device__ __forceinline__ void block_xV(const float *src, int sstride, int n,
-                                         const bf16 *__restrict__ V, int r, float *out,
-                                         int ostride, float *zred)
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    for (int kb = 0; kb < r; kb += 32) {
-        const int k = kb + lane;
-        float part[TT];
-#pragma unroll
-        for (int t = 0; t < TT; ++t) part[t] = 0.f;
-        if (k < r) {
-            for (int i = warp; i < n; i += kWarps) {
-                const float v = bf2f(V[(int64_t)i * r + k]);
-#pragma unroll
-                for (int t = 0; t < TT; ++t) part[t] = fmaf(src[t * sstride + i], v, part[t]);
-            }
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded waits: false after kWaitLimitNs (the status word is then set).
+__device__ __noinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *status, unsigned site)
+{
+    if (mbar_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | site);
+            return false;
         }
-#pragma unroll
-        for (int t = 0; t < TT; ++t) zred[(warp * TT + t) * 32 + lane] = part[t];
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < TT * 32; idx += kThreads) {
-            const int t = idx >> 5, l = idx & 31;
-            if (kb + l < r) {
-                float s = 0.f;
-#pragma unroll
-                for (int w = 0; w < kWarps; ++w) s += zred[(w * TT + t) * 32 + l];
-                out[t * ostride + kb + l] = s;
-            }
-        }
-        __syncthreads();
     }
+    return true;
+}
+
+__device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, unsigned parity, unsigned *status)
+{
+    if (mbar_test_cluster(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_test_cluster(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | kWaitExchange);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Arrive on the mbarrier at the same shared-memory offset in CTA `rank` of
+// this cluster, with release semantics at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint64_t *bar, unsigned rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote) : "memory");
+}
+
+// One 2D tile of a tensor map into shared memory; c0 = column (inner), c1 =
+// row.  Completion is counted on `bar` in bytes.
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void ldmatrix_x4(uint32_t a[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
+                 : "r"(addr));
+}
+
+// D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Cluster barrier split in two: every thread arrives once right after the
+// barriers are initialised (the producer then never waits), and the consumer
+// threads wait only before their first access to a peer CTA.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+
+// Barrier among the 256 consumer threads only (the producer never joins).
+__device__ __forceinline__ void consumer_sync()
+{
+    asm volatile("bar.sync 1, %0;" ::"n"(kThreads) : "memory");
+}
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Start copying nbytes (even) from global `src` into the shared buffer `dst`
+// (16-byte aligned, nbytes + 16 bytes long) and return where src's first byte
+// lands (dst + src % 16, so 16-byte alignment carries over).  The aligned body
+// is copied with cp.async, the unaligned head and tail with 2-byte loads; no
+// byte outside [src, src + nbytes) is read.  Finish with cp_async_wait_all()
+// and a consumer barrier.
+__device__ __forceinline__ const char *prefetch(char *dst, const void *src, int nbytes)
+{
+    const uintptr_t s0 = reinterpret_cast<uintptr_t>(src);
+    const uintptr_t s1 = s0 + (uintptr_t)nbytes;
+    char *d = dst + (s0 & 15);
+    uintptr_t b0 = (s0 + 15) & ~uintptr_t(15), b1 = s1 & ~uintptr_t(15);
+    if (b1 <= b0) b0 = b1 = s1;  // no whole 16-byte chunk: all by elements
+    for (uintptr_t c = b0 + 16 * threadIdx.x; c < b1; c += 16 * kThreads)
+        cp_async16(d + (c - s0), reinterpret_cast<const void *>(c));
+    const int nhead = (int)((b0 < s1 ? b0 : s1) - s0) >> 1;
+    const int ntail = (int)(s1 - (b1 > s0 ? b1 : s0)) >> 1;
+    const uint16_t *g = reinterpret_cast<const uint16_t *>(src);
+    uint16_t *o = reinterpret_cast<uint16_t *>(d);
+    const int tail0 = (int)((b1 > s0 ? b1 : s0) - s0) >> 1;
+    for (int e = threadIdx.x; e < nhead; e += kThreads) o[e] = g[e];
+    if (b1 > b0)
+        for (int e = threadIdx.x; e < ntail; e += kThreads) o[tail0 + e] = g[tail0 + e];
+    return d;
 }
 
 __device__ __forceinline__ float gelu_tanh_f32(float v)
@@ -188,287 +232,743 @@ __device__ __forceinline__ float gelu_tanh_f32(float v)
 }
 
 // ------------------------------------------------------------------------
+// Rank-r helpers (consumer threads 0..255)
+// ------------------------------------------------------------------------
+
+// How 8 consecutive rank values of a row can be loaded: 2 = one 16-byte
+// load, 1 = two 8-byte loads, 0 = element by element.
+__device__ __forceinline__ int vec_mode(const bf16 *p, int r)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    if (r % 8 == 0 && a % 16 == 0) return 2;
+    if (r % 4 == 0 && a % 8 == 0) return 1;
+    return 0;
+}
+
+// v[e] = M[i*r + kc + e] as fp32 for e < 8 (0 where kc + e >= r); M may be in
+// global or shared memory.
+__device__ __forceinline__ void load8(const bf16 *__restrict__ M, int64_t i, int r, int kc, int vm,
+                                      float v[8])
+{
+    const bf16 *p = M + i * r + kc;
+    if (vm == 2) {
+        const uint4 u = *reinterpret_cast<const uint4 *>(p);
+        v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+        v[4] = bf_lo(u.z); v[5] = bf_hi(u.z); v[6] = bf_lo(u.w); v[7] = bf_hi(u.w);
+    } else if (vm == 1) {
+        const uint2 a = *reinterpret_cast<const uint2 *>(p);
+        const uint2 b = (kc + 4 < r) ? *reinterpret_cast<const uint2 *>(p + 4) : make_uint2(0u, 0u);
+        v[0] = bf_lo(a.x); v[1] = bf_hi(a.x); v[2] = bf_lo(a.y); v[3] = bf_hi(a.y);
+        v[4] = bf_lo(b.x); v[5] = bf_hi(b.x); v[6] = bf_lo(b.y); v[7] = bf_hi(b.y);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = (kc + e < r) ? bf2f(p[e]) : 0.f;
+    }
+}
+
+// Warp reduce-scatter of 8 values: returns, in lane l, the sum over all 32
+// lanes of value index l >> 2 (9 shuffles instead of 40).
+__device__ __forceinline__ float warp_reduce8(const float v[8])
+{
+    const int lane = threadIdx.x & 31;
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float a[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const float send = b4 ? v[j] : v[j + 4];
+        const float keep = b4 ? v[j + 4] : v[j];
+        a[j] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
+    }
+    float c[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+        const float send = b3 ? a[j] : a[j + 2];
+        const float keep = b3 ? a[j + 2] : a[j];
+        c[j] = keep + __shfl_xor_sync(0xffffffffu, send, 8);
+    }
+    const float send = b2 ? c[0] : c[1];
+    const float keep = b2 ? c[1] : c[0];
+    float d = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+    d += __shfl_xor_sync(0xffffffffu, d, 2);
+    d += __shfl_xor_sync(0xffffffffu, d, 1);
+    return d;
+}
+
+// out[t*ostride + k] = sum_{i < n} src(t, i) * V[i*r + k] for t < TT,
+// k < r (out may be shared or global memory).  One thread per row i of V,
+// eight ranks per load, several loads in flight per thread; partial sums are
+// reduced across the warp, then across warps in shared memory (zred:
+// kWarps*TT*8 floats).  Contains consumer barriers.
+template <int TT, typename Src>
+__device__ __forceinline__ void block_xV(Src src, int n, const bf16 *__restrict__ V, int r,
+                                         float *out, int ostride, float *zred)
+{
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int vm = vec_mode(V, r);
+    for (int kc = 0; kc < r; kc += 8) {
+        float p[TT][8];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[t][e] = 0.f;
+#pragma unroll 2
+        for (int i = tid; i < n; i += kThreads) {
+            float v[8];
+            load8(V, i, r, kc, vm, v);
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                const float xv = src(t, i);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) p[t][e] = fmaf(xv, v[e], p[t][e]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            const float sum = warp_reduce8(p[t]);
+            if ((lane & 3) == 0) zred[(warp * TT + t) * 8 + (lane >> 2)] = sum;
+        }
+        consumer_sync();
+        for (int idx = tid; idx < TT * 8; idx += kThreads) {
+            const int t = idx >> 3, j = idx & 7;
+            if (kc + j < r) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) sum += zred[(w * TT + t) * 8 + j];
+                out[t * ostride + kc + j] = sum;
+            }
+        }
+        consumer_sync();
+    }
+}
+
+// y[t] += sum_k U[o*r + k] * z[t*zs + k], t < TT (loads of eight ranks at a
+// time, issued ahead of their use).
+template <int TT>
+__device__ __forceinline__ void add_delta(const bf16 *__restrict__ U, int64_t o, int r, int vm,
+                                          const float *z, int zs, float yv[TT])
+{
+#pragma unroll 2
+    for (int kc = 0; kc < r; kc += 8) {
+        float u[8];
+        load8(U, o, r, kc, vm, u);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (kc + e < r)
+#pragma unroll
+                for (int t = 0; t < TT; ++t) yv[t] = fmaf(u[e], z[t * zs + kc + e], yv[t]);
+    }
+}
+
+// ------------------------------------------------------------------------
+// Ring of 16 KB stages shared by the producer thread and the consumer warps
+// ------------------------------------------------------------------------
+struct Ring {
+    char *base;       // nst stages of kStageBytes, 1024-byte aligned
+    uint64_t *full;   // [nst]: producer -> consumers (transaction bytes)
+    uint64_t *empty;  // [nst]: consumers -> producer (kWarps arrivals)
+    int nst;
+    int s;            // current stage
+    unsigned ph;      // parity of the current pass over the ring
+    __device__ __forceinline__ void advance()
+    {
+        if (++s == nst) {
+            s = 0;
+            ph ^= 1u;
+        }
+    }
+};
+
+// Producer (one thread): rows [row0, row0 + 64) x columns [k0, k0 + 64*ktiles)
+// of `map`, two 64x64 boxes per stage.  Rows or columns past the matrix are
+// filled with zeros by the TMA unit.
+__device__ __forceinline__ bool produce_tile(Ring &rg, const CUtensorMap *map, int row0, int k0,
+                                             int ktiles, unsigned *status)
+{
+    for (int kt = 0; kt < ktiles; kt += 2) {
+        if (!mbar_wait(&rg.empty[rg.s], rg.ph ^ 1u, status, kWaitRingEmpty)) return false;
+        const int nb = min(2, ktiles - kt);
+        mbar_expect_tx(&rg.full[rg.s], (unsigned)(nb * kBoxBytes));
+        char *dst = rg.base + (size_t)rg.s * kStageBytes;
+        for (int b = 0; b < nb; ++b) tma_load_2d(dst + b * kBoxBytes, map, k0 + (kt + b) * kBK, row0, &rg.full[rg.s]);
+        rg.advance();
+    }
+    return true;
+}
+
+// Consumers: the tile's stages on the tensor cores.  Warp w owns rows
+// 16*(w&3) .. +15 of the tile and the k-steps of parity (w>>2) of each stage;
+// the two warps of a row group are added at the end.  xb: the tile's x as
+// bf16 pairs, row n (token) at xb + n*xs32 (u32 units), column 0 = the CTA's
+// k0, zero past its K range.  acc[row*ald + n] receives the raw dot products
+// of the 64 rows with the 8*NT columns.  red: 512*NT floats.
+template <int NT>
+__device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_t *xb, int xs32,
+                                             float *red, float *acc, int ald, unsigned *status)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rw = warp & 3, kw = warp >> 2;
+    const int g = lane >> 2, t4 = lane & 3;
+    float c[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+    // ldmatrix row/chunk of this lane (swizzled 128-byte rows)
+    const int lrow = rw * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int lchunk = lane >> 4;
+    bool ok = true;
+    for (int kt = 0; kt < ktiles; kt += 2) {
+        int w_ok = 1;
+        if (lane == 0) w_ok = mbar_wait(&rg.full[rg.s], rg.ph, status, kWaitRingFull);
+        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+        if (!w_ok) {
+            ok = false;
+            break;
+        }
+        const uint32_t sb = smem_u32(rg.base + (size_t)rg.s * kStageBytes);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int step = kw + 2 * q;    // 0..7 within the stage
+            const int box = step >> 2;      // which 64-column box
+            const int kin = step & 3;       // 16-column step inside the box
+            if (kt + box >= ktiles) continue;
+            uint32_t a[4];
+            const int chunk = kin * 2 + lchunk;
+            ldmatrix_x4(a, sb + box * kBoxBytes + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
+            const int kk = (kt + box) * kBK + kin * 16;  // column relative to k0
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                const uint32_t *xr = xb + (nt * 8 + g) * xs32 + (kk >> 1) + t4;
+                mma_16816(c[nt], a, xr[0], xr[4]);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&rg.empty[rg.s]);
+        rg.advance();
+    }
+    // add the two k-halves of every row group and store
+    if (kw == 1) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) red[((rw * NT + nt) * 4 + e) * 32 + lane] = c[nt][e];
+    }
+    consumer_sync();
+    if (kw == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[nt][e] += red[((rw * NT + nt) * 4 + e) * 32 + lane];
+            const int row = rw * 16 + g, col = nt * 8 + 2 * t4;
+            acc[row * ald + col] = c[nt][0];
+            acc[row * ald + col + 1] = c[nt][1];
+            acc[(row + 8) * ald + col] = c[nt][2];
+            acc[(row + 8) * ald + col + 1] = c[nt][3];
+        }
+    }
+    consumer_sync();
+    return ok;
+}
+
+// Deterministic cluster reduction of per-CTA partials held in shared memory.
+// publish: all CTAs signal every peer, then wait until every peer signalled.
+// release: after reading the peers' partials, tell every peer.
+// reclaim: before the CTA exits, wait until every peer has released it.
+struct Exchange {
+    uint64_t *ready;
+    uint64_t *done;
+};
+
+__device__ __forceinline__ void exchange_publish(const Exchange &ex, int KS, unsigned *status)
+{
+    cluster_wait();  // every CTA of the cluster has initialised its barriers
+    consumer_sync();
+    if (threadIdx.x == 0)
+        for (int p = 0; p < KS; ++p) mbar_arrive_remote(ex.ready, (unsigned)p);
+    mbar_wait_cluster(ex.ready, 0, status);
+}
+
+__device__ __forceinline__ void exchange_release(const Exchange &ex, int KS)
+{
+    consumer_sync();
+    if (threadIdx.x == 0)
+        for (int p = 0; p < KS; ++p) mbar_arrive_remote(ex.done, (unsigned)p);
+}
+
+__device__ __forceinline__ void exchange_reclaim(const Exchange &ex, unsigned *status)
+{
+    mbar_wait_cluster(ex.done, 0, status);
+}
+
+// Shared memory: ring (1024-byte aligned) | barriers | floats.
+struct Carve {
+    Ring rg;
+    Exchange ex;
+    char *rest;  // 16-byte aligned, after the barriers
+};
+
+__host__ __device__ constexpr int carve_head_bytes(int nst) { return 1024 + nst * kStageBytes + (2 * nst + 2) * 8 + 16; }
+
+__device__ __forceinline__ Carve carve(char *smem_raw, int nst)
+{
+    // 128-byte swizzled TMA tiles want 1024-byte aligned stages
+    char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    Carve c;
+    c.rg.base = smem;
+    c.rg.nst = nst;
+    c.rg.s = 0;
+    c.rg.ph = 0;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)nst * kStageBytes);
+    c.rg.full = bars;
+    c.rg.empty = bars + nst;
+    c.ex.ready = bars + 2 * nst;
+    c.ex.done = bars + 2 * nst + 1;
+    c.rest = reinterpret_cast<char *>(bars + 2 * nst + 2);
+    c.rest = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(c.rest) + 15) & ~uintptr_t(15));
+    return c;
+}
+
+__device__ __forceinline__ void init_barriers(Carve &c, int KS)
+{
+    for (int i = 0; i < c.rg.nst; ++i) {
+        mbar_init(&c.rg.full[i], 1);
+        mbar_init(&c.rg.empty[i], kWarps);
+    }
+    mbar_init(c.ex.ready, KS);
+    mbar_init(c.ex.done, KS);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// x[t, k0:k0+klen) (bf16, row stride ld) -> xb rows (bf16, xs32 u32 per row),
+// width 64*ktiles (zero past klen); rows t >= T zero.  nrow = 8*NT rows.
+__device__ __forceinline__ void stage_x(const bf16 *__restrict__ x, int64_t ld, int T, int k0, int klen,
+                                        int width, int nrow, uint32_t *xb, int xs32)
+{
+    const int nq = width >> 3;  // 16-byte chunks per row
+    for (int idx = threadIdx.x; idx < nrow * nq; idx += kThreads) {
+        const int t = idx / nq, c = idx - t * nq;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (t < T && 8 * c < klen) v = *reinterpret_cast<const uint4 *>(x + t * ld + k0 + 8 * c);
+        *reinterpret_cast<uint4 *>(xb + t * xs32 + 4 * c) = v;
+    }
+}
+
+// ------------------------------------------------------------------------
 // wl_linear / wl_qkv_fused decode kernel
 // ------------------------------------------------------------------------
 struct DecSeg {
-    const bf16 *W0;
+    CUtensorMap map;  // W0 [out, in], box 64 x 64
     const float *s;
     const bf16 *U;
     const bf16 *V;
     void *y;
     int out;
-    int blk0;  // first row block of this segment
-    int nblk;  // row blocks of this segment
+    int grp0;  // first row group of this segment
+    int ngrp;  // row groups of this segment
 };
 
 struct DecArgs {
+    DecSeg seg[3];
     const bf16 *x;
     int T, in, r, ydt;
-    int KS, Kc;  // K splits (= cluster size) and K elements per split
-    int rmax;    // largest row block
-    int nseg;
-    DecSeg seg[3];
+    int KS, Kc;  // K splits (= cluster size), K elements per split (multiple of 64)
+    int tpc;     // 64-row tiles per row group
+    int nseg, nst, xs32;
+    int vbuf, ubuf;  // shared-memory bytes for the prefetched V slice and U rows (0: read in place)
+    unsigned *status;
 };
 
-template <int TT>
-__host__ __device__ constexpr int dec_zred_floats() { return kWarps * TT * 32; }
-
-template <int TT, int LPR>
-__global__ void __launch_bounds__(kThreads, 2) dec_linear_kernel(const __grid_constant__ DecArgs a)
+template <int NT, int TC>
+__global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid_constant__ DecArgs a)
 {
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(1024) char smem_raw[];
     const int KS = a.KS;
-    const int q = (int)(blockIdx.x % (unsigned)KS);  // rank in the cluster
-    const int b = (int)(blockIdx.x / (unsigned)KS);  // row block
-    const int si = (a.nseg > 2 && b >= a.seg[2].blk0) ? 2 : (a.nseg > 1 && b >= a.seg[1].blk0) ? 1 : 0;
-    const DecSeg sg = si == 0 ? a.seg[0] : (si == 1 ? a.seg[1] : a.seg[2]);
-    const int lb = b - sg.blk0;
-    const int r0 = (int)((int64_t)lb * sg.out / sg.nblk);
-    const int nrows = (int)((int64_t)(lb + 1) * sg.out / sg.nblk) - r0;
+    const int q = (int)(blockIdx.x % (unsigned)KS);
+    const int gi = (int)(blockIdx.x / (unsigned)KS);
+    const int si = (a.nseg > 2 && gi >= a.seg[2].grp0) ? 2 : (a.nseg > 1 && gi >= a.seg[1].grp0) ? 1 : 0;
+    const DecSeg &sg = a.seg[si];
+    const int r0 = (gi - sg.grp0) * a.tpc * kBR;
+    const int nrows = min(sg.out - r0, a.tpc * kBR);
+    const int ntl = (nrows + kBR - 1) / kBR;
     const int k0 = q * a.Kc;
     const int klen = max(0, min(a.in, k0 + a.Kc) - k0);
+    const int ktiles = (klen + kBK - 1) / kBK;
     const int rp = a.r > 0 ? a.r : 1;
+    constexpr int ald = 8 * NT;
 
-    float *xs = smem;
-    float *acc = xs + TT * a.Kc;
-    float *zp = acc + a.rmax * TT;
-    float *zred = zp + TT * rp;
+    Carve c = carve(smem_raw, a.nst);
+    uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
+    float *acc = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *red = acc + a.tpc * kBR * ald;
+    float *zp = red + 512 * NT;  // [ceil8(T)][rp]
+    float *zred = zp + ((a.T + 7) / 8) * 8 * rp;
+    char *sbuf = reinterpret_cast<char *>(zred + 512);
+    char *vbuf = sbuf + a.tpc * kBR * 4 + 16;
+    char *ubuf = vbuf + a.vbuf;
 
-    stage_x_bf16<TT>(a.x, a.in, a.T, k0, klen, a.Kc, xs);
-    __syncthreads();
+    if (threadIdx.x == 0) {
+        init_barriers(c, KS);
+        pdl_trigger();
+    }
+    __syncthreads();           // barriers initialised (this CTA)
+    if (KS > 1) cluster_arrive();  // peers may arrive remotely once all have passed this
 
-    const bf16 *W0 = sg.W0 + (int64_t)r0 * a.in + k0;
-    const int64_t ld = a.in;
-    stream_rows<TT, LPR>([&](int v) { return W0 + v * ld; }, nrows, klen >> 3, xs, a.Kc, acc);
+    if (threadIdx.x >= kThreads) {  // ---------------- producer thread
+        if (threadIdx.x == kThreads && ktiles > 0)
+            for (int tl = 0; tl < ntl; ++tl)
+                if (!produce_tile(c.rg, &sg.map, r0 + tl * kBR, k0, ktiles, a.status)) break;
+        return;
+    }
 
-    if (a.r > 0) block_xV<TT>(xs, a.Kc, klen, sg.V + (int64_t)k0 * a.r, a.r, zp, rp, zred);
-    __syncthreads();
+    // ------------------------------------------------ consumer warps
+    // weight-side operands first (they do not depend on the previous kernel),
+    // so their round trips overlap the x load and the W0 stream
+    const float *sv_p = reinterpret_cast<const float *>(prefetch(sbuf, sg.s + r0, nrows * 4));
+    const bf16 *Vp = sg.V + (int64_t)k0 * a.r;
+    const bf16 *Up = sg.U + (int64_t)r0 * a.r;
+    if (a.r > 0 && a.vbuf > 0) {
+        Vp = reinterpret_cast<const bf16 *>(prefetch(vbuf, Vp, klen * a.r * 2));
+        Up = reinterpret_cast<const bf16 *>(prefetch(ubuf, Up, nrows * a.r * 2));
+    }
+    pdl_wait();  // x comes from the previous kernel on the stream
+    stage_x(a.x, a.in, a.T, k0, klen, ktiles * kBK, 8 * NT, xb, a.xs32);
+    consumer_sync();
+    // W0 first: the ring has been filling since the kernel started
+    for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, acc + tl * kBR * ald, ald, a.status);
+    cp_async_wait_all();
+    consumer_sync();
+    const bf16 *xbh = reinterpret_cast<const bf16 *>(xb);
+    const int xsh = 2 * a.xs32;
+    if (a.r > 0)
+        for (int t0 = 0; t0 < a.T; t0 += TC)
+            block_xV<TC>([&](int t, int i) { return t0 + t < a.T ? bf2f(xbh[(t0 + t) * xsh + i]) : 0.f; },
+                         klen, Vp, a.r, zp + t0 * rp, rp, zred);
 
     // epilogue: p = s*acc + U z_range
+    const int vmU = vec_mode(Up, a.r);
     for (int row = threadIdx.x; row < nrows; row += kThreads) {
         const int o = r0 + row;
-        const float sv = sg.s[o];
-        float yv[TT];
+        const float sv = sv_p[row];
+        for (int t0 = 0; t0 < a.T; t0 += TC) {
+            float yv[TC];
 #pragma unroll
-        for (int t = 0; t < TT; ++t) yv[t] = sv * acc[row * TT + t];
-        const bf16 *Ur = sg.U + (int64_t)o * a.r;
-        for (int k = 0; k < a.r; ++k) {
-            const float u = bf2f(Ur[k]);
+            for (int j = 0; j < TC; ++j) yv[j] = (ktiles > 0 && t0 + j < ald) ? sv * acc[row * ald + t0 + j] : 0.f;
+            if (a.r > 0) add_delta<TC>(Up, row, a.r, vmU, zp + t0 * rp, rp, yv);
 #pragma unroll
-            for (int t = 0; t < TT; ++t) yv[t] = fmaf(u, zp[t * rp + k], yv[t]);
-        }
-        if (KS == 1) {
-#pragma unroll
-            for (int t = 0; t < TT; ++t)
-                if (t < a.T) store_out(sg.y, a.ydt, (int64_t)t * sg.out + o, yv[t]);
-        } else {
-#pragma unroll
-            for (int t = 0; t < TT; ++t) acc[row * TT + t] = yv[t];
+            for (int j = 0; j < TC; ++j) {
+                if (t0 + j >= a.T) break;
+                if (KS == 1)
+                    store_out(sg.y, a.ydt, (int64_t)(t0 + j) * sg.out + o, yv[j]);
+                else
+                    acc[row * ald + t0 + j] = yv[j];
+            }
         }
     }
     if (KS > 1) {
         cg::cluster_group cl = cg::this_cluster();
-        cl.sync();
+        exchange_publish(c.ex, KS, a.status);
         const int lo = (int)((int64_t)q * nrows / KS);
         const int n = (int)((int64_t)(q + 1) * nrows / KS) - lo;
         for (int idx = threadIdx.x; idx < n * a.T; idx += kThreads) {
             const int t = idx / n, row = lo + (idx - t * n);
             float v = 0.f;
-            for (int p = 0; p < KS; ++p) v += cl.map_shared_rank(acc, p)[row * TT + t];
+            for (int p = 0; p < KS; ++p) v += cl.map_shared_rank(acc, p)[row * ald + t];
             store_out(sg.y, a.ydt, (int64_t)t * sg.out + r0 + row, v);
         }
-        cl.sync();
+        exchange_release(c.ex, KS);
+        exchange_reclaim(c.ex, a.status);  // peers are done with this CTA's memory
     }
 }
 
 // ------------------------------------------------------------------------
-// fused GeGLU MLP decode kernel (persistent, two phases)
+// fused GeGLU MLP decode: launch 1 (gate, up -> h, partials of h V_down)
 // ------------------------------------------------------------------------
-struct MlpArgs {
+struct GateUpArgs {
+    CUtensorMap mapg, mapu;
     const bf16 *x;
-    int T, hidden, inter, r, ydt;
-    const bf16 *Wg, *Wu, *Wd;
-    const float *sg, *su, *sd;
-    const bf16 *Ug, *Uu, *Ud, *Vg, *Vu, *Vd;
-    void *y;
-    float *h;          // workspace [kDecodeTT][inter] fp32
-    float *zd;         // workspace [NB1][kDecodeTT][rp] fp32
-    unsigned *bar;     // workspace [2]: arrival count, generation
-    unsigned *status;  // library status word
-    int KS, Kc1, Kc2, NB1, NB2, rmax1, rmax2, hmax, nclus;
-    int xs_f, acc_f;   // smem region sizes (floats)
+    int T, hidden, inter, r;
+    const float *sg, *su;
+    const bf16 *Ug, *Uu, *Vg, *Vu, *Vd;
+    float *h;   // workspace [kTokChunk][inter] fp32
+    float *zd;  // workspace [ngrp*KS][kTokChunk][rp] fp32
+    int KS, Kc, tpc, nst, xs32, hmax;
+    int vbuf, ubuf, dbuf;  // shared-memory bytes per prefetched V slice / U block / V_down rows (0: in place)
+    unsigned *status;
 };
 
-// Grid-wide barrier over all CTAs of the launch (all co-resident).  Bounded:
-// after kWaitLimitNs it records kStatusTimeout and returns false.
-__device__ bool grid_barrier(unsigned *bar, unsigned nblocks, unsigned *status)
+template <int TC>
+__global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid_constant__ GateUpArgs a)
 {
-    __shared__ int ok;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        volatile unsigned *vgen = bar + 1;
-        const unsigned gen = *vgen;
-        __threadfence();
-        const unsigned prev = atomicAdd(bar, 1u);
-        ok = 1;
-        if (prev == nblocks - 1) {
-            atomicExch(bar, 0u);
-            __threadfence();
-            atomicAdd(bar + 1, 1u);
-        } else {
-            const uint64_t t0 = globaltimer_ns();
-            while (*vgen == gen) {
-                __nanosleep(100);
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(status, kStatusTimeout);
-                    ok = 0;
-                    break;
-                }
-            }
-        }
-        __threadfence();
-    }
-    __syncthreads();
-    return ok != 0;
-}
-
-template <int TT, int LPR1, int LPR2>
-__global__ void __launch_bounds__(kThreads, 2) dec_mlp_kernel(const __grid_constant__ MlpArgs a)
-{
-    extern __shared__ __align__(16) float smem[];
-    cg::cluster_group cl = cg::this_cluster();
+    constexpr int NT = 1, ald = 8;
+    extern __shared__ __align__(1024) char smem_raw[];
     const int KS = a.KS;
     const int q = (int)(blockIdx.x % (unsigned)KS);
-    const int cid = (int)(blockIdx.x / (unsigned)KS);
+    const int gi = (int)(blockIdx.x / (unsigned)KS);
     const int rp = a.r > 0 ? a.r : 1;
+    const int j0 = gi * a.tpc * kBR;
+    const int nr = min(a.inter - j0, a.tpc * kBR);
+    const int ntl = (nr + kBR - 1) / kBR;
+    const int k0 = q * a.Kc;
+    const int klen = max(0, min(a.hidden, k0 + a.Kc) - k0);
+    const int ktiles = (klen + kBK - 1) / kBK;
 
-    float *xs = smem;
-    float *acc = xs + a.xs_f;
-    float *zp = acc + a.acc_f;       // [2][TT][rp]
-    float *zred = zp + 2 * TT * rp;  // [kWarps*TT*32]
-    float *zdl = zred + dec_zred_floats<TT>();  // [TT][rp]
-    float *hl = zdl + TT * rp;       // [TT][hmax]
+    Carve c = carve(smem_raw, a.nst);
+    uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
+    float *accg = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *accu = accg + a.tpc * kBR * ald;
+    float *red = accu + a.tpc * kBR * ald;
+    float *zg = red + 512 * NT;   // [8][rp]
+    float *zu = zg + 8 * rp;      // [8][rp]
+    float *zred = zu + 8 * rp;    // [512]
+    float *hl = zred + 512;       // [8][hmax]
+    char *sgb = reinterpret_cast<char *>(hl + 8 * a.hmax);
+    char *sub = sgb + a.tpc * kBR * 4 + 16;
+    char *vgb = sub + a.tpc * kBR * 4 + 16;
+    char *vub = vgb + a.vbuf;
+    char *ugb = vub + a.vbuf;
+    char *uub = ugb + a.ubuf;
+    char *vdb = uub + a.ubuf;
 
-    // ---- phase 1: g, u -> h, and z_down partials -----------------------
-    for (int b = cid; b < a.NB1; b += a.nclus) {
-        const int j0 = (int)((int64_t)b * a.inter / a.NB1);
-        const int nr = (int)((int64_t)(b + 1) * a.inter / a.NB1) - j0;
-        const int k0 = q * a.Kc1;
-        const int klen = max(0, min(a.hidden, k0 + a.Kc1) - k0);
+    if (threadIdx.x == 0) {
+        init_barriers(c, KS);
+        pdl_trigger();
+    }
+    __syncthreads();           // barriers initialised (this CTA)
+    if (KS > 1) cluster_arrive();  // peers may arrive remotely once all have passed this
 
-        stage_x_bf16<TT>(a.x, a.hidden, a.T, k0, klen, a.Kc1, xs);
-        __syncthreads();
-        const bf16 *Wg = a.Wg + (int64_t)j0 * a.hidden + k0;
-        const bf16 *Wu = a.Wu + (int64_t)j0 * a.hidden + k0;
-        const int64_t ld = a.hidden;
-        stream_rows<TT, LPR1>(
-            [&](int v) { return v < nr ? Wg + v * ld : Wu + (v - nr) * ld; }, 2 * nr,
-            klen >> 3, xs, a.Kc1, acc);
-        if (a.r > 0) {
-            block_xV<TT>(xs, a.Kc1, klen, a.Vg + (int64_t)k0 * a.r, a.r, zp, rp, zred);
-            block_xV<TT>(xs, a.Kc1, klen, a.Vu + (int64_t)k0 * a.r, a.r, zp + TT * rp, rp, zred);
-        }
-        __syncthreads();
-        for (int v = threadIdx.x; v < 2 * nr; v += kThreads) {
-            const bool up = v >= nr;
-            const int j = j0 + (up ? v - nr : v);
-            const float sv = up ? a.su[j] : a.sg[j];
-            const bf16 *Ur = (up ? a.Uu : a.Ug) + (int64_t)j * a.r;
-            const float *z = zp + (up ? TT * rp : 0);
-            float yv[TT];
-#pragma unroll
-            for (int t = 0; t < TT; ++t) yv[t] = sv * acc[v * TT + t];
-            for (int k = 0; k < a.r; ++k) {
-                const float u = bf2f(Ur[k]);
-#pragma unroll
-                for (int t = 0; t < TT; ++t) yv[t] = fmaf(u, z[t * rp + k], yv[t]);
+    if (threadIdx.x >= kThreads) {  // ---------------- producer thread
+        if (threadIdx.x == kThreads && ktiles > 0)
+            for (int tl = 0; tl < ntl; ++tl) {
+                if (!produce_tile(c.rg, &a.mapg, j0 + tl * kBR, k0, ktiles, a.status)) break;
+                if (!produce_tile(c.rg, &a.mapu, j0 + tl * kBR, k0, ktiles, a.status)) break;
             }
+        return;
+    }
+
+    // ------------------------------------------------ consumer warps
+    const int lo = (int)((int64_t)q * nr / KS);
+    const int n = (int)((int64_t)(q + 1) * nr / KS) - lo;
+    const float *sgp = reinterpret_cast<const float *>(prefetch(sgb, a.sg + j0, nr * 4));
+    const float *sup = reinterpret_cast<const float *>(prefetch(sub, a.su + j0, nr * 4));
+    const bf16 *Vgp = a.Vg + (int64_t)k0 * a.r, *Vup = a.Vu + (int64_t)k0 * a.r;
+    const bf16 *Ugp = a.Ug + (int64_t)j0 * a.r, *Uup = a.Uu + (int64_t)j0 * a.r;
+    const bf16 *Vdp = a.Vd + (int64_t)(j0 + lo) * a.r;
+    if (a.r > 0 && a.vbuf > 0 && a.dbuf > 0) {
+        Vgp = reinterpret_cast<const bf16 *>(prefetch(vgb, Vgp, klen * a.r * 2));
+        Vup = reinterpret_cast<const bf16 *>(prefetch(vub, Vup, klen * a.r * 2));
+        Ugp = reinterpret_cast<const bf16 *>(prefetch(ugb, Ugp, nr * a.r * 2));
+        Uup = reinterpret_cast<const bf16 *>(prefetch(uub, Uup, nr * a.r * 2));
+        Vdp = reinterpret_cast<const bf16 *>(prefetch(vdb, Vdp, n * a.r * 2));
+    }
+    pdl_wait();
+    stage_x(a.x, a.hidden, a.T, k0, klen, ktiles * kBK, 8 * NT, xb, a.xs32);
+    consumer_sync();
+    for (int tl = 0; tl < ntl && ktiles > 0; ++tl) {
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, accg + tl * kBR * ald, ald, a.status);
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, accu + tl * kBR * ald, ald, a.status);
+    }
+    cp_async_wait_all();
+    consumer_sync();
+    const bf16 *xbh = reinterpret_cast<const bf16 *>(xb);
+    const int xsh = 2 * a.xs32;
+    auto xsrc = [&](int t, int i) { return t < a.T ? bf2f(xbh[t * xsh + i]) : 0.f; };
+    if (a.r > 0) {
+        block_xV<TC>(xsrc, klen, Vgp, a.r, zg, rp, zred);
+        block_xV<TC>(xsrc, klen, Vup, a.r, zu, rp, zred);
+    }
+    // partial g, u over this K range: s*acc + U z_range (in place)
+    const int vmUg = vec_mode(Ugp, a.r), vmUu = vec_mode(Uup, a.r);
+    for (int v = threadIdx.x; v < 2 * nr; v += kThreads) {
+        const bool up = v >= nr;
+        const int row = up ? v - nr : v;
+        float *acc = up ? accu : accg;
+        const float sv = up ? sup[row] : sgp[row];
+        float yv[TC];
 #pragma unroll
-            for (int t = 0; t < TT; ++t) acc[v * TT + t] = yv[t];
-        }
-        cl.sync();
-        // my share of the rows: complete g, u -> h
-        const int lo = (int)((int64_t)q * nr / KS);
-        const int n = (int)((int64_t)(q + 1) * nr / KS) - lo;
-        for (int idx = threadIdx.x; idx < n * TT; idx += kThreads) {
+        for (int t = 0; t < TC; ++t) yv[t] = ktiles > 0 ? sv * acc[row * ald + t] : 0.f;
+        if (a.r > 0) add_delta<TC>(up ? Uup : Ugp, row, a.r, up ? vmUu : vmUg, up ? zu : zg, rp, yv);
+#pragma unroll
+        for (int t = 0; t < TC; ++t) acc[row * ald + t] = yv[t];
+    }
+    // complete g, u for this CTA's share of the rows, then h = gelu(g) * u
+    if (KS > 1) {
+        cg::cluster_group cl = cg::this_cluster();
+        exchange_publish(c.ex, KS, a.status);
+        for (int idx = threadIdx.x; idx < n * TC; idx += kThreads) {
             const int t = idx / n, v = lo + (idx - t * n);
             float g = 0.f, u = 0.f;
             for (int p = 0; p < KS; ++p) {
-                const float *pa = cl.map_shared_rank(acc, p);
-                g += pa[v * TT + t];
-                u += pa[(nr + v) * TT + t];
+                g += cl.map_shared_rank(accg, p)[v * ald + t];
+                u += cl.map_shared_rank(accu, p)[v * ald + t];
             }
             const float hv = t < a.T ? gelu_tanh_f32(g) * u : 0.f;
             hl[t * a.hmax + (v - lo)] = hv;
             if (t < a.T) a.h[(int64_t)t * a.inter + j0 + v] = hv;
         }
-        __syncthreads();
-        if (a.r > 0) block_xV<TT>(hl, a.hmax, n, a.Vd + (int64_t)(j0 + lo) * a.r, a.r, zdl, rp, zred);
-        cl.sync();
-        if (q == 0 && a.r > 0) {
-            float *dst = a.zd + (int64_t)b * kDecodeTT * rp;
-            for (int idx = threadIdx.x; idx < TT * a.r; idx += kThreads) {
-                const int t = idx / a.r, k = idx - t * a.r;
-                float s = 0.f;
-                for (int p = 0; p < KS; ++p) s += cl.map_shared_rank(zdl, p)[t * rp + k];
-                dst[t * rp + k] = s;
-            }
+        exchange_release(c.ex, KS);
+    } else {
+        consumer_sync();
+        for (int idx = threadIdx.x; idx < n * TC; idx += kThreads) {
+            const int t = idx / n, v = lo + (idx - t * n);
+            const float hv = t < a.T ? gelu_tanh_f32(accg[v * ald + t]) * accu[v * ald + t] : 0.f;
+            hl[t * a.hmax + (v - lo)] = hv;
+            if (t < a.T) a.h[(int64_t)t * a.inter + j0 + v] = hv;
         }
-        cl.sync();
+        consumer_sync();
+    }
+    // partial z_down = sum over this CTA's rows of h V_down, to the workspace
+    if (a.r > 0)
+        block_xV<TC>([&](int t, int i) { return hl[t * a.hmax + i]; }, n, Vdp, a.r,
+                     a.zd + ((int64_t)gi * KS + q) * kTokChunk * rp, rp, zred);
+    if (KS > 1) exchange_reclaim(c.ex, a.status);
+}
+
+// ------------------------------------------------------------------------
+// fused GeGLU MLP decode: launch 2 (y = wl(h; down))
+// ------------------------------------------------------------------------
+struct DownArgs {
+    CUtensorMap mapd;
+    const float *h;   // [kTokChunk][inter] fp32, written by launch 1
+    const float *zd;  // [nzd][kTokChunk][rp] partials of h V_down
+    int nzd;
+    int T, inter, hidden, r, ydt;
+    const float *sd;
+    const bf16 *Ud;
+    void *y;
+    int KS, Kc, tpc, nst, xs32;
+    int ubuf;  // shared-memory bytes for the prefetched U rows (0: read in place)
+    unsigned *status;
+};
+
+// x columns of the down product: token t's h as bf16 (column t) plus the
+// rounding remainder h - bf16(h) as bf16 (column T + t); their sum carries h
+// to about 16 bits, enough for fp32-output accuracy.
+template <int NT, int TC>
+__global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_constant__ DownArgs a)
+{
+    constexpr int ald = 8 * NT;
+    extern __shared__ __align__(1024) char smem_raw[];
+    const int KS = a.KS;
+    const int q = (int)(blockIdx.x % (unsigned)KS);
+    const int gi = (int)(blockIdx.x / (unsigned)KS);
+    const int rp = a.r > 0 ? a.r : 1;
+    const int o0 = gi * a.tpc * kBR;
+    const int nr = min(a.hidden - o0, a.tpc * kBR);
+    const int ntl = (nr + kBR - 1) / kBR;
+    const int k0 = q * a.Kc;
+    const int klen = max(0, min(a.inter, k0 + a.Kc) - k0);
+    const int ktiles = (klen + kBK - 1) / kBK;
+
+    Carve c = carve(smem_raw, a.nst);
+    uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
+    float *acc = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *red = acc + a.tpc * kBR * ald;
+    float *zp = red + 512 * NT;    // [8][rp]
+    float *zred = zp + 8 * rp;     // [kThreads]
+    char *sbuf = reinterpret_cast<char *>(zred + kThreads);
+    char *ubuf = sbuf + a.tpc * kBR * 4 + 16;
+
+    if (threadIdx.x == 0) {
+        init_barriers(c, KS);
+        pdl_trigger();
+    }
+    __syncthreads();           // barriers initialised (this CTA)
+    if (KS > 1) cluster_arrive();  // peers may arrive remotely once all have passed this
+
+    if (threadIdx.x >= kThreads) {  // ---------------- producer: W_down does not depend on h
+        if (threadIdx.x == kThreads && ktiles > 0)
+            for (int tl = 0; tl < ntl; ++tl)
+                if (!produce_tile(c.rg, &a.mapd, o0 + tl * kBR, k0, ktiles, a.status)) break;
+        return;
     }
 
-    // On a timeout the status word is set and the CTA carries on (its output
-    // is then meaningless): returning early could strand cluster peers at a
-    // cluster barrier, while carrying on keeps every wait bounded.
-    grid_barrier(a.bar, gridDim.x, a.status);
-
-    // ---- phase 2: y = wl(h; down) ---------------------------------------
-    for (int b = cid; b < a.NB2; b += a.nclus) {
-        const int o0 = (int)((int64_t)b * a.hidden / a.NB2);
-        const int nr = (int)((int64_t)(b + 1) * a.hidden / a.NB2) - o0;
-        const int k0 = q * a.Kc2;
-        const int klen = max(0, min(a.inter, k0 + a.Kc2) - k0);
-
-        stage_x_f32<TT>(a.h, a.inter, a.T, k0, klen, a.Kc2, xs);
-        if (q == 0 && a.r > 0) {
-            for (int idx = threadIdx.x; idx < TT * a.r; idx += kThreads) {
-                const int t = idx / a.r, k = idx - t * a.r;
-                float s = 0.f;
-                for (int p = 0; p < a.NB1; ++p) s += __ldcg(a.zd + ((int64_t)p * kDecodeTT + t) * rp + k);
-                zp[t * rp + k] = s;
+    // ------------------------------------------------ consumer warps
+    const int rr = (q == 0) ? a.r : 0;  // the low-rank term is added by one rank
+    const float *sdp = reinterpret_cast<const float *>(prefetch(sbuf, a.sd + o0, nr * 4));
+    const bf16 *Udp = a.Ud + (int64_t)o0 * a.r;
+    if (rr > 0 && a.ubuf > 0) Udp = reinterpret_cast<const bf16 *>(prefetch(ubuf, Udp, nr * a.r * 2));
+    pdl_wait();  // h and the partials come from launch 1
+    {
+        const int width = ktiles * kBK;
+        const int nq = width >> 2;  // 4-column groups
+        bf16 *xbh = reinterpret_cast<bf16 *>(xb);
+        const int xsh = 2 * a.xs32;
+        for (int idx = threadIdx.x; idx < 8 * NT * nq; idx += kThreads) {
+            const int n = idx / nq, cq = idx - n * nq;
+            const int t = n < a.T ? n : n - a.T;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (n < 2 * a.T && 4 * cq < klen)
+                v = __ldcg(reinterpret_cast<const float4 *>(a.h + (int64_t)t * a.inter + k0 + 4 * cq));
+            const float e[4] = {v.x, v.y, v.z, v.w};
+            for (int j = 0; j < 4; ++j) {
+                const bf16 hi = __float2bfloat16_rn(e[j]);
+                xbh[n * xsh + 4 * cq + j] = n < a.T ? hi : __float2bfloat16_rn(e[j] - __bfloat162float(hi));
             }
         }
-        __syncthreads();
-        const bf16 *Wd = a.Wd + (int64_t)o0 * a.inter + k0;
-        const int64_t ld = a.inter;
-        stream_rows<TT, LPR2>([&](int v) { return Wd + v * ld; }, nr, klen >> 3, xs, a.Kc2, acc);
-        __syncthreads();
-        const int rr = (q == 0) ? a.r : 0;  // the low-rank term is added once
-        for (int row = threadIdx.x; row < nr; row += kThreads) {
-            const int o = o0 + row;
-            const float sv = a.sd[o];
-            float yv[TT];
-#pragma unroll
-            for (int t = 0; t < TT; ++t) yv[t] = sv * acc[row * TT + t];
-            const bf16 *Ur = a.Ud + (int64_t)o * a.r;
-            for (int k = 0; k < rr; ++k) {
-                const float u = bf2f(Ur[k]);
-#pragma unroll
-                for (int t = 0; t < TT; ++t) yv[t] = fmaf(u, zp[t * rp + k], yv[t]);
-            }
-#pragma unroll
-            for (int t = 0; t < TT; ++t) acc[row * TT + t] = yv[t];
+    }
+    const int vmU = vec_mode(Udp, a.r);
+    // z_down[t][k] = sum over the nzd partials in a fixed order: threads split
+    // the partials into chunks (loads in flight together), chunk sums are then
+    // added in chunk order.
+    const int nout = TC * rr;
+    if (nout > 0 && nout <= kThreads) {
+        const int nch = kThreads / nout;
+        const int ch = threadIdx.x / nout, cc = threadIdx.x - ch * nout;
+        if (ch < nch) {
+            const int t = cc / rr, k = cc - t * rr;
+            float s = 0.f;
+#pragma unroll 4
+            for (int p = ch; p < a.nzd; p += nch) s += __ldcg(a.zd + ((int64_t)p * kTokChunk + t) * rp + k);
+            zred[ch * nout + cc] = s;
         }
-        cl.sync();
+        consumer_sync();
+        for (int c2 = threadIdx.x; c2 < nout; c2 += kThreads) {
+            float s = 0.f;
+            for (int j = 0; j < nch; ++j) s += zred[j * nout + c2];
+            zp[(c2 / rr) * rp + (c2 % rr)] = s;
+        }
+    } else if (nout > 0) {
+        for (int c2 = threadIdx.x; c2 < nout; c2 += kThreads) {
+            const int t = c2 / rr, k = c2 - t * rr;
+            float s = 0.f;
+#pragma unroll 4
+            for (int p = 0; p < a.nzd; ++p) s += __ldcg(a.zd + ((int64_t)p * kTokChunk + t) * rp + k);
+            zp[t * rp + k] = s;
+        }
+    }
+    cp_async_wait_all();
+    consumer_sync();
+    for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, acc + tl * kBR * ald, ald, a.status);
+    for (int row = threadIdx.x; row < nr; row += kThreads) {
+        const int o = o0 + row;
+        const float sv = sdp[row];
+        float yv[TC];
+#pragma unroll
+        for (int t = 0; t < TC; ++t)
+            yv[t] = (ktiles > 0 && t < a.T) ? sv * (acc[row * ald + t] + acc[row * ald + a.T + t]) : 0.f;
+        if (rr > 0) add_delta<TC>(Udp, row, rr, vmU, zp, rp, yv);
+#pragma unroll
+        for (int t = 0; t < TC; ++t) {
+            if (t >= a.T) break;
+            if (KS == 1)
+                store_out(a.y, a.ydt, (int64_t)t * a.hidden + o, yv[t]);
+            else
+                acc[row * ald + t] = yv[t];
+        }
+    }
+    if (KS > 1) {
+        cg::cluster_group cl = cg::this_cluster();
+        exchange_publish(c.ex, KS, a.status);
         const int lo = (int)((int64_t)q * nr / KS);
         const int n = (int)((int64_t)(q + 1) * nr / KS) - lo;
         for (int idx = threadIdx.x; idx < n * a.T; idx += kThreads) {
             const int t = idx / n, row = lo + (idx - t * n);
             float v = 0.f;
-            for (int p = 0; p < KS; ++p) v += cl.map_shared_rank(acc, p)[row * TT + t];
+            for (int p = 0; p < KS; ++p) v += cl.map_shared_rank(acc, p)[row * ald + t];
             store_out(a.y, a.ydt, (int64_t)t * a.hidden + o0 + row, v);
         }
-        cl.sync();
+        exchange_release(c.ex, KS);
+        exchange_reclaim(c.ex, a.status);
     }
 }
 
@@ -476,287 +976,295 @@ __global__ void __launch_bounds__(kThreads, 2) dec_mlp_kernel(const __grid_const
 // host side
 // ------------------------------------------------------------------------
 static inline int round_up(int v, int m) { return (v + m - 1) / m * m; }
-static inline int lpr_for(int nck) { return nck >= 64 ? 32 : (nck >= 32 ? 16 : 8); }
-static inline int lpr_index(int lpr) { return lpr == 32 ? 2 : (lpr == 16 ? 1 : 0); }
-static inline int tt_for(int64_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : 8; }
-static inline int tt_index(int tt) { return tt == 1 ? 0 : tt == 2 ? 1 : tt == 4 ? 2 : 3; }
+static inline int cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+constexpr int kSmemTarget = 112 * 1024;  // two CTAs (of successive kernels) share an SM
+constexpr int kMaxPartials = 512;        // z_down partials (one per gate/up CTA)
+constexpr int kPrefetchBudget = 24 * 1024;  // shared memory for prefetched rank-r operands
 
 typedef void (*dec_fn)(DecArgs);
-typedef void (*mlp_fn)(MlpArgs);
+typedef void (*gu_fn)(GateUpArgs);
+typedef void (*dn_fn)(DownArgs);
+// [token chunk 1 or 8][n-tiles 1, 2, 4, 8]; one token uses the TC = 1 forms
+static dec_fn g_dec[2][4] = {{dec_linear_kernel<1, 1>, nullptr, nullptr, nullptr},
+                             {dec_linear_kernel<1, 8>, dec_linear_kernel<2, 8>, dec_linear_kernel<4, 8>,
+                              dec_linear_kernel<8, 8>}};
+static gu_fn g_gu[2] = {dec_gateup_kernel<1>, dec_gateup_kernel<8>};
+static dn_fn g_dn[2][2] = {{dec_down_kernel<1, 1>, nullptr}, {dec_down_kernel<1, 8>, dec_down_kernel<2, 8>}};
 
-template <int TT>
-static void fill_dec(dec_fn *row)
-{
-    row[0] = dec_linear_kernel<TT, 8>;
-    row[1] = dec_linear_kernel<TT, 16>;
-    row[2] = dec_linear_kernel<TT, 32>;
-}
-static dec_fn g_dec[4][3];
-
-template <int TT, int L1>
-static void fill_mlp2(mlp_fn *row)
-{
-    row[0] = dec_mlp_kernel<TT, L1, 8>;
-    row[1] = dec_mlp_kernel<TT, L1, 16>;
-    row[2] = dec_mlp_kernel<TT, L1, 32>;
-}
-template <int TT>
-static void fill_mlp(mlp_fn (*tab)[3])
-{
-    fill_mlp2<TT, 8>(tab[0]);
-    fill_mlp2<TT, 16>(tab[1]);
-    fill_mlp2<TT, 32>(tab[2]);
-}
-static mlp_fn g_mlp[4][3][3];
+static inline int nt_index(int nt) { return nt <= 1 ? 0 : nt <= 2 ? 1 : nt <= 4 ? 2 : 3; }
+static inline int nt_round(int nt) { return nt <= 1 ? 1 : nt <= 2 ? 2 : nt <= 4 ? 4 : 8; }
 
 static std::mutex g_mu;
-static std::unordered_map<uint64_t, int> g_smem_set;  // (device, fn) -> bytes set
+static std::unordered_map<uint64_t, int> g_attr_set;  // (device, fn) -> done
 
-static wl_status ensure_smem(const void *fn, int bytes, const DeviceInfo *di)
+static wl_status ensure_attrs(const void *fn, int bytes, const DeviceInfo *di)
 {
     if (bytes > di->max_smem_optin)
         return fail(WL_ERR_UNSUPPORTED, "decode kernel needs %d bytes of shared memory, device allows %d",
                     bytes, di->max_smem_optin);
     std::lock_guard<std::mutex> lk(g_mu);
     const uint64_t key = ((uint64_t)di->device << 56) ^ (uint64_t)(uintptr_t)fn;
-    auto it = g_smem_set.find(key);
-    if (it != g_smem_set.end() && it->second >= bytes) return WL_OK;
-    const int want = di->max_smem_optin;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, want);
+    if (g_attr_set.count(key)) return WL_OK;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, di->max_smem_optin);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic smem)");
-    e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(non-portable cluster)");
-    g_smem_set[key] = want;
+    g_attr_set[key] = 1;
     return WL_OK;
 }
 
-static void init_tables()
-{
-    static std::once_flag once;
-    std::call_once(once, [] {
-        fill_dec<1>(g_dec[0]);
-        fill_dec<2>(g_dec[1]);
-        fill_dec<4>(g_dec[2]);
-        fill_dec<8>(g_dec[3]);
-        fill_mlp<1>(g_mlp[0]);
-        fill_mlp<2>(g_mlp[1]);
-        fill_mlp<4>(g_mlp[2]);
-        fill_mlp<8>(g_mlp[3]);
-    });
-}
-
-static wl_status launch_with_cluster(const void *fn, int grid, int KS, int smem, cudaStream_t st,
-                                     void **args)
+static wl_status launch(const void *fn, int grid, int KS, int smem, cudaStream_t st, void **args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kDecThreads);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)KS;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     cudaError_t e = cudaLaunchKernelExC(&cfg, fn, args);
     if (e != cudaSuccess) return cuda_fail(e, "decode kernel launch");
     return WL_OK;
 }
 
-// One launch over up to kDecodeTT tokens.
+// Work split of `ntile` 64-row tiles with K = in:
+//   tpc   tiles per row group: each group forms z = x V once, so more tiles
+//         per group keep the rank-r operand's traffic small next to W0;
+//   KS    K splits (cluster size), chosen to give about one CTA per SM;
+//   Kc    K elements per split, a multiple of 64 (whole TMA boxes).
+struct Split {
+    int tpc, ngrp, KS, Kc;
+};
+
+static Split plan_split(int ntile, int in, int r_eff, int max_kc, const DeviceInfo *di)
+{
+    Split s;
+    s.tpc = cdiv(r_eff, 12);
+    if (s.tpc < 1) s.tpc = 1;
+    if (s.tpc > 8) s.tpc = 8;
+    for (;;) {
+        s.ngrp = cdiv(ntile, s.tpc);
+        int ks = 1;
+        while (ks < 8 && (s.ngrp * ks < di->sm_count || round_up(cdiv(in, ks), kBK) > max_kc) &&
+               cdiv(in, 2 * ks) >= kBK)
+            ks *= 2;
+        s.Kc = round_up(cdiv(in, ks), kBK);
+        s.KS = cdiv(in, s.Kc);
+        if (s.ngrp * s.KS * 4 >= di->sm_count * 3 || s.tpc == 1) break;
+        s.tpc = (s.tpc + 1) / 2;
+    }
+    return s;
+}
+
+// Ring stages that fit next to `other` bytes of shared memory.
+static int ring_stages(int other, const DeviceInfo *di)
+{
+    int n = (kSmemTarget - other - 1024) / kStageBytes;
+    if (n > 6) n = 6;
+    if (n < 3) {  // does not fit next to another CTA: use one SM's worth
+        n = (di->max_smem_optin - other - 1024) / kStageBytes;
+        if (n > 6) n = 6;
+    }
+    return n;
+}
+
+// x row stride in u32: 16-byte multiple, odd number of 16-byte units (keeps
+// the tensor-core operand reads free of shared-memory bank conflicts).
+static inline int x_stride32(int width)
+{
+    int u16 = width / 8;  // 16-byte units of bf16
+    if ((u16 & 1) == 0) u16 += 1;
+    return u16 * 4;
+}
+
 static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, void *const *y,
-                                 int T, int in, int r, int ydt, cudaStream_t st,
+                                 int64_t T, int64_t in, int64_t r, int ydt, cudaStream_t st,
                                  const DeviceInfo *di)
 {
-    const int TT = tt_for(T);
-    int64_t rows = 0;
-    for (int j = 0; j < nproj; ++j) rows += proj[j].out;
-    const int target = 2 * di->sm_count;
-
-    // K split (cluster size): enough row work per CTA, x slice small enough
-    // for shared memory, and few enough row blocks that the rank-r operand V
-    // (re-read by every row block) stays small next to W0.
-    int KS = 1;
-    auto kc_of = [&](int ks) { return round_up((in + ks - 1) / ks, 8); };
-    while (KS < 8 && TT * kc_of(KS) * 4 > 96 * 1024) KS *= 2;
-    while (KS < 8) {
-        const int64_t nb = target / KS;
-        const bool few_rows = rows / nb < 16;
-        const bool v_heavy = r > 0 && nb * 4 * (int64_t)r > rows;
-        if ((few_rows || v_heavy) && kc_of(2 * KS) >= 64) KS *= 2;
-        else break;
-    }
-    const int Kc = kc_of(KS);
-    int64_t nb_total = target / KS;
-    if (nb_total < nproj) nb_total = nproj;
+    wl_status s = WL_OK;
+    const int NT = nt_round(cdiv(T, 8));
+    int ntile = 0;
+    for (int j = 0; j < nproj; ++j) ntile += cdiv(proj[j].out, kBR);
+    // keep x (8*NT rows of K columns) within about 48 KB
+    int max_kc = (48 * 1024) / (8 * NT * 2);
+    max_kc = max_kc < kBK ? kBK : (max_kc / kBK) * kBK;
+    Split sp = plan_split(ntile, (int)in, (int)r, max_kc, di);
 
     DecArgs a = {};
     a.x = x;
-    a.T = T;
-    a.in = in;
-    a.r = r;
+    a.T = (int)T;
+    a.in = (int)in;
+    a.r = (int)r;
     a.ydt = ydt;
-    a.KS = KS;
-    a.Kc = Kc;
+    a.KS = sp.KS;
+    a.Kc = sp.Kc;
+    a.tpc = sp.tpc;
     a.nseg = nproj;
-    int blk = 0, rmax = 1;
+    a.status = di->status;
+    a.xs32 = x_stride32(sp.Kc);
+    int grp = 0;
     for (int j = 0; j < nproj; ++j) {
-        int nblk = (int)((nb_total * proj[j].out + rows - 1) / rows);
-        if (nblk < 1) nblk = 1;
-        if (nblk > proj[j].out) nblk = (int)proj[j].out;
         DecSeg &sg = a.seg[j];
-        sg.W0 = static_cast<const bf16 *>(proj[j].W0);
+        s = tmap_2d_bf16(proj[j].W0, in, proj[j].out, in, kBK, kBR, &sg.map);
+        if (s != WL_OK) return s;
         sg.s = proj[j].s;
         sg.U = static_cast<const bf16 *>(proj[j].U);
         sg.V = static_cast<const bf16 *>(proj[j].V);
         sg.y = y[j];
         sg.out = (int)proj[j].out;
-        sg.blk0 = blk;
-        sg.nblk = nblk;
-        blk += nblk;
-        const int rm = (int)((proj[j].out + nblk - 1) / nblk);
-        if (rm > rmax) rmax = rm;
+        sg.grp0 = grp;
+        sg.ngrp = cdiv(cdiv(proj[j].out, kBR), sp.tpc);
+        grp += sg.ngrp;
     }
-    a.rmax = rmax;
-    const int rp = r > 0 ? r : 1;
-    const int smem = 4 * (TT * Kc + rmax * TT + TT * rp + kWarps * TT * 32);
-    const dec_fn fn = g_dec[tt_index(TT)][lpr_index(lpr_for(Kc / 8))];
-    wl_status s = ensure_smem((const void *)fn, smem, di);
+    const int rp = r > 0 ? (int)r : 1;
+    // prefetch the V slice and U rows into shared memory when they are small
+    const int vb = round_up(sp.Kc * (int)r * 2 + 16, 16), ub = round_up(sp.tpc * kBR * (int)r * 2 + 16, 16);
+    if (r > 0 && vb + ub <= kPrefetchBudget) {
+        a.vbuf = vb;
+        a.ubuf = ub;
+    }
+    const int other = 8 * NT * a.xs32 * 4 + 4 * (sp.tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp + 512) +
+                      sp.tpc * kBR * 4 + 16 + a.vbuf + a.ubuf;
+    a.nst = ring_stages(other, di);
+    const int smem = carve_head_bytes(a.nst) + other;
+    if (a.nst < 2) return fail(WL_ERR_UNSUPPORTED, "decode: shapes too large for shared memory");
+    const dec_fn fn = g_dec[T == 1 ? 0 : 1][nt_index(NT)];
+    s = ensure_attrs((const void *)fn, smem, di);
     if (s != WL_OK) return s;
     void *args[] = {&a};
-    return launch_with_cluster((const void *)fn, blk * KS, KS, smem, st, args);
+    return launch((const void *)fn, grp * sp.KS, sp.KS, smem, st, args);
 }
+
+// Decode path for up to 64 tokens per launch (W0 streamed once per launch).
+constexpr int64_t kDecodeMaxT = 64;
 
 wl_status launch_decode_linear(const bf16 *x, const wl_proj *proj, int nproj, void *const *y,
                                int64_t T, int64_t in, int64_t r, int ydt, cudaStream_t st)
 {
-    init_tables();
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
     if (!di) return s;
     const int es = ydt == WL_OUT_F32 ? 4 : 2;
-    for (int64_t t0 = 0; t0 < T; t0 += kDecodeTT) {
-        const int Tc = (int)((T - t0) < kDecodeTT ? (T - t0) : kDecodeTT);
+    for (int64_t t0 = 0; t0 < T; t0 += kDecodeMaxT) {
+        const int64_t Tc = (T - t0) < kDecodeMaxT ? (T - t0) : kDecodeMaxT;
         void *yc[3];
         for (int j = 0; j < nproj; ++j)
             yc[j] = static_cast<char *>(y[j]) + (size_t)t0 * (size_t)proj[j].out * es;
-        s = dec_linear_once(x + t0 * in, proj, nproj, yc, Tc, (int)in, (int)r, ydt, st, di);
+        s = dec_linear_once(x + t0 * in, proj, nproj, yc, Tc, in, r, ydt, st, di);
         if (s != WL_OK) return s;
     }
     return WL_OK;
 }
 
 // ---- MLP ---------------------------------------------------------------
-static constexpr int kMlpKS = 8;
-static constexpr int kMaxNB1 = 512;
-
 size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r)
 {
     (void)hidden;
     const int64_t rp = r > 0 ? r : 1;
     auto al = [](int64_t v) { return (v + 255) / 256 * 256; };
-    return (size_t)(256 + al(kDecodeTT * inter * 4) + al((int64_t)kMaxNB1 * kDecodeTT * rp * 4));
-}
-
-static std::unordered_map<uint64_t, int> g_max_clusters;
-
-static wl_status max_active_clusters(const void *fn, int smem, const DeviceInfo *di, int *out)
-{
-    const uint64_t key = ((uint64_t)di->device << 56) ^ ((uint64_t)(uintptr_t)fn << 8) ^ (uint64_t)smem;
-    {
-        std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_max_clusters.find(key);
-        if (it != g_max_clusters.end()) {
-            *out = it->second;
-            return WL_OK;
-        }
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(kMlpKS * 64);
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = (size_t)smem;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kMlpKS;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveClusters");
-    if (n < 1) return fail(WL_ERR_UNSUPPORTED, "MLP kernel cannot place a cluster of %d CTAs", kMlpKS);
-    std::lock_guard<std::mutex> lk(g_mu);
-    g_max_clusters[key] = n;
-    *out = n;
-    return WL_OK;
+    return (size_t)(256 + al(kTokChunk * inter * 4) + al((int64_t)kMaxPartials * kTokChunk * rp * 4));
 }
 
 static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj &up,
                               const wl_proj &down, void *y, int T, int hidden, int inter, int r,
                               char *ws, int ydt, cudaStream_t st, const DeviceInfo *di)
 {
-    const int TT = tt_for(T);
-    const int KS = kMlpKS;
-    const int Kc1 = round_up((hidden + KS - 1) / KS, 8);
-    const int Kc2 = round_up((inter + KS - 1) / KS, 8);
     const int rp = r > 0 ? r : 1;
+    float *h = reinterpret_cast<float *>(ws + 256);
+    float *zd = reinterpret_cast<float *>(ws + 256 + ((int64_t)kTokChunk * inter * 4 + 255) / 256 * 256);
 
-    int nclus = (2 * di->sm_count) / KS;
-    int NB1 = nclus < kMaxNB1 ? nclus : kMaxNB1;
-    if (NB1 > inter) NB1 = inter;
-    int NB2 = nclus < hidden ? nclus : hidden;
-    const int rmax1 = (inter + NB1 - 1) / NB1;
-    const int rmax2 = (hidden + NB2 - 1) / NB2;
-    const int hmax = (rmax1 + KS - 1) / KS + 1;
-    MlpArgs a = {};
-    a.x = x;
-    a.T = T;
-    a.hidden = hidden;
-    a.inter = inter;
-    a.r = r;
-    a.ydt = ydt;
-    a.Wg = static_cast<const bf16 *>(gate.W0);
-    a.Wu = static_cast<const bf16 *>(up.W0);
-    a.Wd = static_cast<const bf16 *>(down.W0);
-    a.sg = gate.s;
-    a.su = up.s;
-    a.sd = down.s;
-    a.Ug = static_cast<const bf16 *>(gate.U);
-    a.Uu = static_cast<const bf16 *>(up.U);
-    a.Ud = static_cast<const bf16 *>(down.U);
-    a.Vg = static_cast<const bf16 *>(gate.V);
-    a.Vu = static_cast<const bf16 *>(up.V);
-    a.Vd = static_cast<const bf16 *>(down.V);
-    a.y = y;
-    a.bar = reinterpret_cast<unsigned *>(ws);
-    a.h = reinterpret_cast<float *>(ws + 256);
-    a.zd = reinterpret_cast<float *>(ws + 256 + ((int64_t)kDecodeTT * inter * 4 + 255) / 256 * 256);
-    a.status = di->status;
-    a.KS = KS;
-    a.Kc1 = Kc1;
-    a.Kc2 = Kc2;
-    a.NB1 = NB1;
-    a.NB2 = NB2;
-    a.rmax1 = rmax1;
-    a.rmax2 = rmax2;
-    a.hmax = hmax;
-    a.xs_f = TT * (Kc1 > Kc2 ? Kc1 : Kc2);
-    a.acc_f = TT * (2 * rmax1 > rmax2 ? 2 * rmax1 : rmax2);
-    const int smem = 4 * (a.xs_f + a.acc_f + 2 * TT * rp + kWarps * TT * 32 + TT * rp + TT * hmax);
-    const mlp_fn fn = g_mlp[tt_index(TT)][lpr_index(lpr_for(Kc1 / 8))][lpr_index(lpr_for(Kc2 / 8))];
-    wl_status s = ensure_smem((const void *)fn, smem, di);
+    // launch 1: gate and up tiles, h, partials of h V_down
+    GateUpArgs g = {};
+    Split sg = plan_split(cdiv(inter, kBR), hidden, 2 * r, 48 * 1024 / 16, di);
+    while (cdiv(inter, kBR * sg.tpc) * sg.KS > kMaxPartials) sg.tpc *= 2;
+    sg.ngrp = cdiv(cdiv(inter, kBR), sg.tpc);
+    wl_status s = tmap_2d_bf16(gate.W0, hidden, inter, hidden, kBK, kBR, &g.mapg);
     if (s != WL_OK) return s;
-    int maxc = 0;
-    s = max_active_clusters((const void *)fn, smem, di, &maxc);
+    s = tmap_2d_bf16(up.W0, hidden, inter, hidden, kBK, kBR, &g.mapu);
     if (s != WL_OK) return s;
-    // every CTA of the launch must be resident at once (grid barrier)
-    if (nclus > maxc) nclus = maxc;
-    a.nclus = nclus;
-    void *args[] = {&a};
-    return launch_with_cluster((const void *)fn, nclus * KS, KS, smem, st, args);
+    g.x = x;
+    g.T = T;
+    g.hidden = hidden;
+    g.inter = inter;
+    g.r = r;
+    g.sg = gate.s;
+    g.su = up.s;
+    g.Ug = static_cast<const bf16 *>(gate.U);
+    g.Uu = static_cast<const bf16 *>(up.U);
+    g.Vg = static_cast<const bf16 *>(gate.V);
+    g.Vu = static_cast<const bf16 *>(up.V);
+    g.Vd = static_cast<const bf16 *>(down.V);
+    g.h = h;
+    g.zd = zd;
+    g.KS = sg.KS;
+    g.Kc = sg.Kc;
+    g.tpc = sg.tpc;
+    g.xs32 = x_stride32(sg.Kc);
+    g.hmax = cdiv(sg.tpc * kBR, sg.KS) + 1;
+    g.status = di->status;
+    {
+        const int vb = round_up(sg.Kc * r * 2 + 16, 16), ub = round_up(sg.tpc * kBR * r * 2 + 16, 16);
+        const int db = round_up(g.hmax * r * 2 + 16, 16);
+        if (r > 0 && 2 * vb + 2 * ub + db <= kPrefetchBudget) {
+            g.vbuf = vb;
+            g.ubuf = ub;
+            g.dbuf = db;
+        }
+    }
+    const int gother = 8 * g.xs32 * 4 + 4 * (2 * sg.tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * g.hmax) +
+                       2 * (sg.tpc * kBR * 4 + 16) + 2 * g.vbuf + 2 * g.ubuf + g.dbuf;
+    g.nst = ring_stages(gother, di);
+    if (g.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
+    const int gsmem = carve_head_bytes(g.nst) + gother;
+    const gu_fn gfn = g_gu[T == 1 ? 0 : 1];
+    s = ensure_attrs((const void *)gfn, gsmem, di);
+    if (s != WL_OK) return s;
+    void *gargs[] = {&g};
+    s = launch((const void *)gfn, sg.ngrp * sg.KS, sg.KS, gsmem, st, gargs);
+    if (s != WL_OK) return s;
+
+    // launch 2: down tiles, input h as bf16 hi/lo columns
+    DownArgs d = {};
+    const int NT = nt_round(cdiv(2 * T, 8));
+    Split sd = plan_split(cdiv(hidden, kBR), inter, r, (48 * 1024) / (8 * NT * 2) / kBK * kBK, di);
+    s = tmap_2d_bf16(down.W0, inter, hidden, inter, kBK, kBR, &d.mapd);
+    if (s != WL_OK) return s;
+    d.h = h;
+    d.zd = zd;
+    d.nzd = sg.ngrp * sg.KS;
+    d.T = T;
+    d.inter = inter;
+    d.hidden = hidden;
+    d.r = r;
+    d.ydt = ydt;
+    d.sd = down.s;
+    d.Ud = static_cast<const bf16 *>(down.U);
+    d.y = y;
+    d.KS = sd.KS;
+    d.Kc = sd.Kc;
+    d.tpc = sd.tpc;
+    d.xs32 = x_stride32(sd.Kc);
+    d.status = di->status;
+    {
+        const int ub = round_up(sd.tpc * kBR * r * 2 + 16, 16);
+        if (r > 0 && ub <= kPrefetchBudget) d.ubuf = ub;
+    }
+    const int dother = 8 * NT * d.xs32 * 4 + 4 * (sd.tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) +
+                       sd.tpc * kBR * 4 + 16 + d.ubuf;
+    d.nst = ring_stages(dother, di);
+    if (d.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
+    const int dsmem = carve_head_bytes(d.nst) + dother;
+    const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
+    s = ensure_attrs((const void *)dfn, dsmem, di);
+    if (s != WL_OK) return s;
+    void *dargs[] = {&d};
+    return launch((const void *)dfn, sd.ngrp * sd.KS, sd.KS, dsmem, st, dargs);
 }
 
 wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up,
@@ -764,15 +1272,14 @@ wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &u
                             int64_t inter, int64_t r, void *ws, size_t ws_bytes, int ydt,
                             cudaStream_t st)
 {
-    init_tables();
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
     if (!di) return s;
     if (ws_bytes < decode_mlp_workspace_bytes(hidden, inter, r))
         return fail(WL_ERR_WORKSPACE, "MLP workspace too small");
     const int es = ydt == WL_OUT_F32 ? 4 : 2;
-    for (int64_t t0 = 0; t0 < T; t0 += kDecodeTT) {
-        const int Tc = (int)((T - t0) < kDecodeTT ? (T - t0) : kDecodeTT);
+    for (int64_t t0 = 0; t0 < T; t0 += kTokChunk) {
+        const int Tc = (int)((T - t0) < kTokChunk ? (T - t0) : kTokChunk);
         s = dec_mlp_once(x + t0 * hidden, gate, up, down,
                          static_cast<char *>(y) + (size_t)t0 * (size_t)hidden * es, Tc,
                          (int)hidden, (int)inter, (int)r, static_cast<char *>(ws), ydt, st, di);

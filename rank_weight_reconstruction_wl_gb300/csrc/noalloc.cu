@@ -66,10 +66,8 @@ extern "C" wl_status wl_mlp_geglu_fused_noalloc(const void *x, wl_proj gate, wl_
     void *scratch = nullptr;
     wl_status st = scratch_address(&scratch);
     if (st != WL_OK) return st;
-    // The scratch keeps whatever the previous call left.  Its first 256 bytes
-    // hold the grid-barrier words, which must start at zero.
-    cudaError_t e = cudaMemsetAsync(scratch, 0, 256, static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "clear built-in scratch");
+    // The scratch keeps whatever the previous call left; the MLP writes every
+    // part of it that it later reads, so nothing has to be cleared.
     return wl_mlp_geglu_fused(x, gate, up, down, y, T, hidden, inter, r, scratch,
                               kNoAllocScratchBytes, ydt, stream);
 }

@@ -1,0 +1,85 @@
+// tmap.cu -- TMA tensor maps for the kernels' 2D tile loads.
+//
+// A tensor map describes a row-major bf16 matrix [outer, inner] in global
+// memory and the box (tile) one cp.async.bulk.tensor instruction copies into
+// shared memory, with 128-byte swizzling so that tiles can be read from shared
+// memory without bank conflicts.  Encoding one costs host time, so maps are
+// cached: a map depends only on (address, sizes, box), so a cache hit is always
+// a valid map, whatever the memory holds.
+#include <cuda.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "wl_internal.cuh"
+
+namespace wl {
+
+typedef CUresult (*encode_tiled_fn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                    const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                    const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static encode_tiled_fn g_encode = nullptr;
+static std::mutex g_tmap_mu;
+
+struct TmapKey {
+    uintptr_t base;
+    int64_t inner, outer, ld;
+    int box_inner, box_outer;
+    bool operator==(const TmapKey &o) const
+    {
+        return base == o.base && inner == o.inner && outer == o.outer && ld == o.ld &&
+               box_inner == o.box_inner && box_outer == o.box_outer;
+    }
+};
+struct TmapKeyHash {
+    size_t operator()(const TmapKey &k) const
+    {
+        uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
+        h ^= (uint64_t)k.inner + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.outer + 0x85EBCA77C2B2AE63ull + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.ld * 31 + (uint64_t)(k.box_inner * 1024 + k.box_outer) + (h << 6) + (h >> 2);
+        return (size_t)h;
+    }
+};
+static std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
+
+wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
+                       int box_inner, int box_outer, CUtensorMap *out)
+{
+    std::lock_guard<std::mutex> lk(g_tmap_mu);
+    if (!g_encode) {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                         cudaEnableDefault, &q);
+        if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn)
+            return fail(WL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+        g_encode = reinterpret_cast<encode_tiled_fn>(fn);
+    }
+    const TmapKey key{reinterpret_cast<uintptr_t>(base), inner, outer, ld_elems, box_inner, box_outer};
+    auto it = g_tmaps.find(key);
+    if (it != g_tmaps.end()) {
+        *out = it->second;
+        return WL_OK;
+    }
+    if (g_tmaps.size() > 4096) g_tmaps.clear();
+    CUtensorMap m;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld_elems * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return fail(WL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%lld, %lld] matrix", (int)r,
+                    (long long)outer, (long long)inner);
+    g_tmaps.emplace(key, m);
+    *out = m;
+    return WL_OK;
+}
+
+}  // namespace wl

@@ -239,7 +239,11 @@ wl_status wl_device_status(void *stream)
         const unsigned zero = 0;
         e = cudaMemcpyToSymbol(g_status_word, &zero, sizeof zero);
         if (e != cudaSuccess) return cuda_fail(e, "clear status word");
-        if (word & kStatusTimeout) return fail(WL_ERR_TIMEOUT, "a bounded device-side wait gave up");
+        if (word & kStatusTimeout)
+            return fail(WL_ERR_TIMEOUT, "a bounded device-side wait gave up (%s%s%s)",
+                        (word & kWaitRingFull) ? " ring-full" : "",
+                        (word & kWaitRingEmpty) ? " ring-empty" : "",
+                        (word & kWaitExchange) ? " cluster-exchange" : "");
     }
     return WL_OK;
 }

@@ -2,6 +2,7 @@
 // the translation units of libwl.so.  Nothing here is part of the C ABI.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -43,8 +44,12 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-// Device status bits (OR-ed into the library's status word).
+// Device status bits (OR-ed into the library's status word): kStatusTimeout
+// plus one bit naming the kind of wait that gave up.
 constexpr unsigned kStatusTimeout = 1u;
+constexpr unsigned kWaitRingFull = 2u;    // consumer waiting for a loaded ring stage
+constexpr unsigned kWaitRingEmpty = 4u;   // producer waiting for a free ring stage
+constexpr unsigned kWaitExchange = 8u;    // waiting for cluster peers' partial sums
 
 // Upper bound of every spin-wait in this library.  A wait that runs longer
 // sets kStatusTimeout and returns instead of waiting further.
@@ -69,6 +74,11 @@ struct DeviceInfo {
 
 // Per-device facts of the current device, queried once per device.
 const DeviceInfo *device_info(wl_status *st);
+
+// 2D tensor map of a row-major bf16 matrix [outer, inner] with row stride
+// ld_elems, box [box_outer, box_inner], 128-byte swizzle (cached).
+wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
+                       int box_inner, int box_outer, CUtensorMap *out);
 
 // Record a message for wl_last_error() and return the status.
 wl_status fail(wl_status st, const char *fmt, ...);
