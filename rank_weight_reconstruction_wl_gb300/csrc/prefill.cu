@@ -1,0 +1,521 @@
+// prefill.cu -- large-T weightless projections on the 5th-generation tensor
+// cores (tcgen05, accumulators in tensor memory), fed by TMA.
+//
+// Computes ("In-kernel reconstruction", formula section and "The GEMM path")
+//     y = s[None,:] * (x W0^T) + z U^T,   z = x V
+// for a tile of 128 tokens x 256 output rows per CTA:
+//   * the main product x W0^T (M = 128 tokens, N = 256 rows, K = in) runs as
+//     tcgen05.mma kind::f16 (bf16 in, fp32 accumulate) into TMEM columns
+//     [0, 256);
+//   * z = x V is formed in the same K loop by a second MMA of the same x
+//     tile against V^T (N = r rounded up to 16) into TMEM columns [256, ...);
+//     V^T is written into swizzled shared memory by the epilogue warps while
+//     the main loop runs (V is [in, r], so its transpose is not a TMA tile);
+//   * the epilogue splits z into bf16 hi + lo parts (z = hi + lo to about 16
+//     bits) and runs the rank-r delta [hi | lo] [U | U]^T as one more MMA into
+//     TMEM columns [256, 512), then forms s * acc + delta in fp32 and casts
+//     once ("The GEMM path": the final combine is done in float32).
+//
+// Warp roles (192 threads): warp 0 = TMA producer, warp 1 = TMEM owner and
+// MMA issuer (one elected thread), warps 2..5 = V^T writer during the main
+// loop, then the epilogue (warp w reads TMEM lanes 32*(w%4) .. +31).
+// Every mbarrier wait is bounded; on a timeout the status word is set and the
+// CTA winds down.
+#include <mutex>
+#include <unordered_map>
+
+#include "wl_internal.cuh"
+
+namespace wl {
+
+constexpr int kPfThreads = 192;
+constexpr int kBM = 128;            // tokens per tile
+constexpr int kBN = 256;            // output rows per tile
+constexpr int kBKp = 64;            // k per stage (one 128-byte swizzle atom)
+constexpr int kATile = kBM * 128;   // 16 KB
+constexpr int kBTile = kBN * 128;   // 32 KB
+constexpr uint32_t kTmemCols = 512;
+
+// ------------------------------------------------------------------ PTX --
+__device__ __forceinline__ uint32_t s32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void pf_mbar_init(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(s32(bar)), "r"(count));
+}
+__device__ __forceinline__ void pf_expect_tx(uint64_t *bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(s32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void pf_arrive(uint64_t *bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(s32(bar)) : "memory");
+}
+__device__ __forceinline__ bool pf_test(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(s32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __noinline__ bool pf_wait(uint64_t *bar, unsigned parity, unsigned *status, unsigned site)
+{
+    if (pf_test(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!pf_test(bar, parity)) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | site);
+            return false;
+        }
+    }
+    return true;
+}
+
+__device__ __forceinline__ void pf_tma_2d(void *dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(s32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(s32(bar))
+        : "memory");
+}
+
+// Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
+// 128 bytes in 8-row (1024-byte) groups.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr)
+{
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor: kind::f16 with bf16 A and B, fp32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma(uint32_t dtmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(dtmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc));
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(s32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16])
+{
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+// Byte offset of element (row, k) in a K-major tile with 128-byte swizzle:
+// atoms of 8 rows x 128 bytes (1024 B); atom columns of 64 elements, each
+// `rows` x 128 bytes.
+__device__ __forceinline__ uint32_t swz(int row, int k, int rows)
+{
+    const int a = k >> 6, kk = k & 63;
+    return (uint32_t)(a * rows * 128 + (row >> 3) * 1024 + (row & 7) * 128 + ((((kk >> 3) ^ (row & 7)) << 4)) +
+                      (kk & 7) * 2);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi)
+{
+    const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t *>(&h);
+}
+
+// ---------------------------------------------------------------- kernel --
+struct PfSeg {
+    CUtensorMap mapb;  // W0 [out, in], box 64 x 256
+    const float *s;
+    const bf16 *U;
+    const bf16 *V;
+    void *y;
+    int out;
+    int ntile0;  // first n-tile of this segment
+};
+
+struct PfArgs {
+    PfSeg seg[3];
+    CUtensorMap mapa;  // x [T, Ktot] (Ktot = in, or 2*in for hi/lo inputs), box 64 x 128
+    int nseg;
+    int T, in, Ktot, r, ydt;
+    int rpad, Kz, nst, stage_bytes, full_count;
+    unsigned *status;
+};
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PfArgs a)
+{
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *smem = smem_raw + ((1024u - (s32(smem_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x, nt = blockIdx.y;
+    const int si = (a.nseg > 2 && nt >= a.seg[2].ntile0) ? 2 : (a.nseg > 1 && nt >= a.seg[1].ntile0) ? 1 : 0;
+    const PfSeg &sg = a.seg[si];
+    const int m0 = mt * kBM, n0 = (nt - sg.ntile0) * kBN;
+    const int r = a.r;
+    const int ktiles = (a.Ktot + kBKp - 1) / kBKp;
+    const int vt_bytes = a.rpad * 128;
+
+    // shared memory: stages | barriers | tmem holder | s tile
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)a.nst * a.stage_bytes);
+    uint64_t *full = bars, *empty = bars + a.nst;
+    uint64_t *acc_full = bars + 2 * a.nst, *z_ready = acc_full + 1, *d_ready = acc_full + 2;
+    uint32_t *tmem_hold = reinterpret_cast<uint32_t *>(acc_full + 3);
+    volatile int &abort_flag = *reinterpret_cast<volatile int *>(tmem_hold + 1);
+    float *s_tile = reinterpret_cast<float *>(tmem_hold + 4);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.nst; ++i) {
+            pf_mbar_init(&full[i], a.full_count);
+            pf_mbar_init(&empty[i], 1);
+        }
+        pf_mbar_init(acc_full, 1);
+        pf_mbar_init(z_ready, 1);
+        pf_mbar_init(d_ready, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s32(tmem_hold)),
+                     "r"(kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // zero the padding rows [r, rpad) of every stage's V^T tile once
+    if (r > 0 && warp >= 2) {
+        for (int st = 0; st < a.nst; ++st) {
+            char *vt = smem + (size_t)st * a.stage_bytes + kATile + kBTile;
+            for (int i = threadIdx.x - 64; i < vt_bytes / 16; i += 128) {
+                const int row = (i * 16) / 128;
+                if (row >= r) reinterpret_cast<uint4 *>(vt)[i] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        fence_async_smem();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_hold;
+    const uint32_t t_main = tmem, t_aux = tmem + kBN;  // columns [0,256) and [256,512)
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer
+        if (lane == 0) {
+            int s = 0;
+            unsigned ph = 0;
+            for (int kt = 0; kt < ktiles; ++kt) {
+                if (!pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty)) {
+                    abort_flag = 1;
+                    break;
+                }
+                char *st = smem + (size_t)s * a.stage_bytes;
+                pf_expect_tx(&full[s], kATile + kBTile);
+                const int kc = kt * kBKp;
+                pf_tma_2d(st, &a.mapa, kc, m0, &full[s]);
+                pf_tma_2d(st + kATile, &sg.mapb, kc % a.in, n0, &full[s]);
+                if (++s == a.nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_main = idesc_bf16(kBM, kBN);
+            const uint32_t id_z = idesc_bf16(kBM, a.rpad > 0 ? a.rpad : 16);
+            int s = 0;
+            unsigned ph = 0;
+            bool ok = true;
+            for (int kt = 0; kt < ktiles; ++kt) {
+                if (!pf_wait(&full[s], ph, a.status, kWaitRingFull)) {
+                    ok = false;
+                    abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sa = s32(smem + (size_t)s * a.stage_bytes);
+                const uint32_t sb = sa + kATile, sv = sb + kBTile;
+#pragma unroll
+                for (int k = 0; k < kBKp / 16; ++k) {
+                    const uint64_t da = sdesc(sa + 32 * k);
+                    const uint32_t accum = (kt > 0 || k > 0) ? 1u : 0u;
+                    umma(t_main, da, sdesc(sb + 32 * k), id_main, accum);
+                    if (r > 0) umma(t_aux, da, sdesc(sv + 32 * k), id_z, accum);
+                }
+                umma_commit(&empty[s]);  // frees the stage when these MMAs are done
+                if (++s == a.nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit(acc_full);
+            if (ok && r > 0) {
+                // rank-r delta: [z_hi | z_lo] [U | U]^T into columns [256, 512)
+                if (pf_wait(z_ready, 0, a.status, kWaitRingFull)) {
+                    tc_fence_after();
+                    const uint32_t saz = s32(smem);                          // A_z at stage memory start
+                    const uint32_t sbu = saz + (uint32_t)(a.Kz / 64) * kATile;  // B_u after it
+                    const uint32_t id_d = idesc_bf16(kBM, kBN);
+                    for (int kd = 0; kd < a.Kz / 16; ++kd) {
+                        const int at = kd >> 2, kin = kd & 3;
+                        umma(t_aux, sdesc(saz + at * kATile + 32 * kin), sdesc(sbu + at * kBTile + 32 * kin), id_d,
+                             kd > 0 ? 1u : 0u);
+                    }
+                    umma_commit(d_ready);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------ V^T writer, then epilogue
+        const int et = threadIdx.x - 64;  // 0..127
+        const int erow = (warp & 3) * 32 + lane;  // TMEM lane = tile row (token)
+        if (r > 0) {
+            int s = 0;
+            unsigned ph = 0;
+            const int nch = (a.rpad < r ? a.rpad : r) * 8;  // (row j, 8-column chunk c) pairs, j < r
+            for (int kt = 0; kt < ktiles; ++kt) {
+                int ok = 1;
+                if (et == 0) ok = pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty);
+                if (et == 0 && !ok) abort_flag = 1;
+                epi_sync();
+                if (abort_flag) break;
+                char *vt = smem + (size_t)s * a.stage_bytes + kATile + kBTile;
+                const int kb = kt * kBKp;
+                for (int idx = et; idx < nch; idx += 128) {
+                    const int j = idx >> 3, c = idx & 7;
+                    float v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int kglob = kb + 8 * c + e;  // position along Ktot; V row kglob mod in
+                        v[e] = kglob < a.Ktot ? bf2f(sg.V[(int64_t)(kglob % a.in) * r + j]) : 0.f;
+                    }
+                    uint4 pk = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                                          pack_bf16(v[6], v[7]));
+                    *reinterpret_cast<uint4 *>(vt + swz(j, 8 * c, a.rpad)) = pk;
+                }
+                fence_async_smem();
+                epi_sync();
+                if (et == 0) pf_arrive(&full[s]);
+                if (++s == a.nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        // s of this tile's rows
+        for (int i = et; i < kBN; i += 128) s_tile[i] = (n0 + i < sg.out) ? sg.s[n0 + i] : 0.f;
+
+        int ok = 1;
+        if (et == 0) ok = pf_wait(acc_full, 0, a.status, kWaitRingFull);
+        if (et == 0 && !ok) abort_flag = 1;
+        epi_sync();
+        tc_fence_after();
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        if (r > 0 && !abort_flag) {
+            // z (fp32) -> A_z = [hi | lo | 0] for this row; U rows -> B_u = [U | U | 0]
+            char *az = smem;
+            char *bu = smem + (size_t)(a.Kz / 64) * kATile;
+            float z[16];
+            for (int cz = 0; cz < a.rpad; cz += 16) {
+                tmem_ld16(t_aux + lane_off + cz, z);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {  // two 8-column groups of this 16-column load
+                    const int k = cz + 8 * h;
+                    if (k >= r) break;
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int ka = k + 2 * e, kb2 = ka + 1;
+                        const float za = ka < r ? z[8 * h + 2 * e] : 0.f;
+                        const float zb = kb2 < r ? z[8 * h + 2 * e + 1] : 0.f;
+                        const float ha = __bfloat162float(__float2bfloat16_rn(za));
+                        const float hb = __bfloat162float(__float2bfloat16_rn(zb));
+                        hi[e] = pack_bf16(ha, hb);
+                        lo[e] = pack_bf16(za - ha, zb - hb);
+                    }
+                    // hi part at columns [k, k+8), lo part at [r + k, r + k + 8):
+                    // write element by element where r is not a multiple of 8
+                    if ((r & 7) == 0) {
+                        *reinterpret_cast<uint4 *>(az + swz(erow, k, kBM)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+                        *reinterpret_cast<uint4 *>(az + swz(erow, r + k, kBM)) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                    } else {
+                        const bf16 *hp = reinterpret_cast<const bf16 *>(hi);
+                        const bf16 *lp = reinterpret_cast<const bf16 *>(lo);
+                        for (int e = 0; e < 8 && k + e < r; ++e) {
+                            *reinterpret_cast<bf16 *>(az + swz(erow, k + e, kBM)) = hp[e];
+                            *reinterpret_cast<bf16 *>(az + swz(erow, r + k + e, kBM)) = lp[e];
+                        }
+                    }
+                }
+            }
+            for (int k = 2 * r; k < a.Kz; ++k) *reinterpret_cast<bf16 *>(az + swz(erow, k, kBM)) = __float2bfloat16_rn(0.f);
+            for (int n = et; n < kBN; n += 128) {
+                const bool in_range = n0 + n < sg.out;
+                const bf16 *Ur = sg.U + (int64_t)(n0 + n) * r;
+                for (int kc = 0; kc < a.Kz; kc += 8) {
+                    uint16_t v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int k = kc + e;
+                        v[e] = (in_range && k < 2 * r) ? reinterpret_cast<const uint16_t *>(Ur)[k < r ? k : k - r] : 0;
+                    }
+                    *reinterpret_cast<uint4 *>(bu + swz(n, kc, kBN)) =
+                        make_uint4(v[0] | (uint32_t)v[1] << 16, v[2] | (uint32_t)v[3] << 16,
+                                   v[4] | (uint32_t)v[5] << 16, v[6] | (uint32_t)v[7] << 16);
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            epi_sync();
+            if (et == 0) pf_arrive(z_ready);
+            int ok2 = 1;
+            if (et == 0) ok2 = pf_wait(d_ready, 0, a.status, kWaitRingFull);
+            if (et == 0 && !ok2) abort_flag = 1;
+            epi_sync();
+            tc_fence_after();
+        }
+        if (!abort_flag) {
+            // y = s * acc + delta, one tile row per thread
+            const int m = m0 + erow;
+            const bool row_ok = m < a.T;
+            const int es = a.ydt == WL_OUT_F32 ? 4 : 2;
+            for (int c = 0; c < kBN; c += 16) {
+                float acc[16], dl[16];
+                tmem_ld16(t_main + lane_off + c, acc);
+                if (r > 0) tmem_ld16(t_aux + lane_off + c, dl);
+                else
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) dl[i] = 0.f;
+                if (!row_ok || n0 + c >= sg.out) continue;
+                float yv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) yv[i] = fmaf(s_tile[c + i], acc[i], dl[i]);
+                const int nvalid = sg.out - (n0 + c);
+                char *dst = static_cast<char *>(sg.y) + ((int64_t)m * sg.out + n0 + c) * es;
+                const bool vec = nvalid >= 16 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0);
+                if (a.ydt == WL_OUT_F32) {
+                    if (vec) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            reinterpret_cast<float4 *>(dst)[q] =
+                                make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+                    } else {
+                        for (int i = 0; i < 16 && i < nvalid; ++i) reinterpret_cast<float *>(dst)[i] = yv[i];
+                    }
+                } else {
+                    if (vec) {
+#pragma unroll
+                        for (int q = 0; q < 2; ++q)
+                            reinterpret_cast<uint4 *>(dst)[q] =
+                                make_uint4(pack_bf16(yv[8 * q], yv[8 * q + 1]), pack_bf16(yv[8 * q + 2], yv[8 * q + 3]),
+                                           pack_bf16(yv[8 * q + 4], yv[8 * q + 5]), pack_bf16(yv[8 * q + 6], yv[8 * q + 7]));
+                    } else {
+                        for (int i = 0; i < 16 && i < nvalid; ++i)
+                            reinterpret_cast<bf16 *>(dst)[i] = __float2bfloat16_rn(yv[i]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------------ host --
+static std::mutex g_pf_mu;
+static std::unordered_map<int, int> g_pf_attr;
+
+wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
+                         int64_t in, int64_t Ktot, int64_t r, int ydt, cudaStream_t st)
+{
+    wl_status s = WL_OK;
+    const DeviceInfo *di = device_info(&s);
+    if (!di) return s;
+    if (r > 128) return fail(WL_ERR_UNSUPPORTED, "prefill: r > 128");
+    if (Ktot != in && (Ktot != 2 * in || in % kBKp != 0))
+        return fail(WL_ERR_UNSUPPORTED, "prefill: hi/lo input needs in %% 64 == 0");
+    PfArgs a = {};
+    a.nseg = nproj;
+    a.T = (int)T;
+    a.in = (int)in;
+    a.Ktot = (int)Ktot;
+    a.r = (int)r;
+    a.ydt = ydt;
+    a.rpad = r > 0 ? (int)((r + 15) / 16 * 16) : 0;
+    a.Kz = r > 0 ? (int)((2 * r + 63) / 64 * 64) : 0;
+    a.status = di->status;
+    a.full_count = r > 0 ? 2 : 1;
+    a.stage_bytes = kATile + kBTile + a.rpad * 128;
+    s = tmap_2d_bf16(x, Ktot, T, Ktot, kBKp, kBM, &a.mapa);
+    if (s != WL_OK) return s;
+    int ntile = 0;
+    for (int j = 0; j < nproj; ++j) {
+        PfSeg &sg = a.seg[j];
+        s = tmap_2d_bf16(proj[j].W0, in, proj[j].out, in, kBKp, kBN, &sg.mapb);
+        if (s != WL_OK) return s;
+        sg.s = proj[j].s;
+        sg.U = static_cast<const bf16 *>(proj[j].U);
+        sg.V = static_cast<const bf16 *>(proj[j].V);
+        sg.y = y[j];
+        sg.out = (int)proj[j].out;
+        sg.ntile0 = ntile;
+        ntile += (int)((proj[j].out + kBN - 1) / kBN);
+    }
+    // stages: as many as fit; the epilogue's A_z / B_u tiles reuse the stages
+    const int extra = 1024 + (2 * 8 + 3) * 8 + 16 + kBN * 4 + 64;
+    int nst = (di->max_smem_optin - extra) / a.stage_bytes;
+    if (nst > 4) nst = 4;
+    const int need_epi = (a.Kz / 64) * (kATile + kBTile);
+    while (nst * a.stage_bytes < need_epi) ++nst;
+    if (nst < 2 || nst * a.stage_bytes + extra > di->max_smem_optin)
+        return fail(WL_ERR_UNSUPPORTED, "prefill: r=%lld needs more shared memory than the device has", (long long)r);
+    a.nst = nst;
+    const int smem = nst * a.stage_bytes + extra;
+    {
+        std::lock_guard<std::mutex> lk(g_pf_mu);
+        if (!g_pf_attr.count(di->device)) {
+            cudaError_t e = cudaFuncSetAttribute((const void *)prefill_kernel,
+                                                 cudaFuncAttributeMaxDynamicSharedMemorySize, di->max_smem_optin);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill)");
+            g_pf_attr[di->device] = 1;
+        }
+    }
+    const dim3 grid((unsigned)((T + kBM - 1) / kBM), (unsigned)ntile);
+    prefill_kernel<<<grid, kPfThreads, smem, st>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return WL_OK;
+}
+
+}  // namespace wl

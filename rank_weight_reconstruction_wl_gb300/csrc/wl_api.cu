@@ -87,6 +87,10 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 
 static constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
+// Token counts up to this run the HBM-streaming decode kernels; larger ones
+// run the tensor-core prefill kernel.
+static constexpr int64_t kDecodeMaxTokens = 64;
+
 static wl_status check_dims(int64_t T, int64_t in, int64_t out, int64_t r)
 {
     if (T < 1 || T > kMaxDim) return fail(WL_ERR_INVALID_ARG, "T must be in [1, 2^30], got %lld", (long long)T);
@@ -147,6 +151,9 @@ wl_status wl_linear(const void *x, const void *W0, const float *s, const void *U
     WL_TRY(begin());
     wl_proj p = {W0, s, U, V, out};
     void *ys[1] = {y};
+    if (T > kDecodeMaxTokens)
+        return launch_prefill(static_cast<const bf16 *>(x), &p, 1, ys, T, in, in, r, ydt,
+                              static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), &p, 1, ys, T, in, r, ydt,
                                 static_cast<cudaStream_t>(stream));
 }
@@ -164,6 +171,9 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
         WL_TRY(check_theta(names[j], ps[j].W0, ps[j].s, ps[j].U, ps[j].V, r));
     }
     WL_TRY(begin());
+    if (T > kDecodeMaxTokens)
+        return launch_prefill(static_cast<const bf16 *>(x), ps, 3, ys, T, in, in, r, ydt,
+                              static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), ps, 3, ys, T, in, r, ydt,
                                 static_cast<cudaStream_t>(stream));
 }

@@ -364,3 +364,23 @@ def test_f64_to_bf16_agrees_with_torch_on_fp32_values(orc):
     a32 = rng.standard_normal(5000).astype(np.float32)
     want = wl_synth.bf16_bits(torch.from_numpy(a32).to(torch.bfloat16))
     assert np.array_equal(orc.f64_to_bf16(a32.astype(np.float64)), want)
+
+
+def test_bf16_error_measure():
+    """The bf16 parity measure: correctly rounded outputs score 0, a one-step
+    flip next to a rounding midpoint scores about the distance to it, and an
+    output two steps off scores about one and a half steps."""
+    from tests.parity import bf16_ulp
+    import torch as _t
+    ref = np.array([1.0 + 2 ** -9, 3.0, 2.0 + 2 ** -7 + 1e-9])
+    y_ok = _t.tensor([1.0, 3.0, 2.0 + 2 ** -6]).to(_t.bfloat16)
+    yv = y_ok.double().numpy()
+    assert np.array_equal(bf16_ulp(np.array([1.0, 3.0, 2.0])), np.array([2 ** -7, 2 ** -6, 2 ** -6]))
+    d = np.maximum(0.0, np.abs(yv - ref) - 0.5 * bf16_ulp(yv))
+    assert np.max(d) < 1e-8
+    y_flip = np.array([1.0, 3.0, 2.0])          # the other side of the midpoint
+    d = np.maximum(0.0, np.abs(y_flip - ref) - 0.5 * bf16_ulp(y_flip))
+    assert d[2] < 2e-9
+    y_bad = np.array([1.0 + 2 * 2 ** -7, 3.0, 2.0])
+    d = np.maximum(0.0, np.abs(y_bad - ref) - 0.5 * bf16_ulp(y_bad))
+    assert abs(d[0] - (2 * 2 ** -7 - 2 ** -9 - 2 ** -8)) < 1e-12
