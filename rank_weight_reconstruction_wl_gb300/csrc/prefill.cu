@@ -133,6 +133,28 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16])
 }
 
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ void pf_cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Four floats at the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ float4 ld_peer4(const float *p, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(s32(p)), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(ra)
+                 : "memory");
+    return v;
+}
 
 // Byte offset of element (row, k) in a K-major tile with 128-byte swizzle:
 // atoms of 8 rows x 128 bytes (1024 B); atom columns of 64 elements, each
@@ -163,12 +185,15 @@ struct PfSeg {
 
 struct PfArgs {
     PfSeg seg[3];
-    CUtensorMap mapa;  // x [T, Ktot] (Ktot = in, or 2*in for hi/lo inputs), box 64 x 128
+    CUtensorMap mapa;  // x [T, Ktot], box 64 x 128
     int nseg;
-    int T, in, Ktot, r, ydt;
+    int T, in, Ktot, kmod, r, ydt;  // K position k maps to W0 column / V row k % kmod (< in)
     int rpad, Kz, nst, stage_bytes, full_count;
+    int ns, kts;  // K splits (= cluster size along z) and k-tiles per split
     unsigned *status;
 };
+
+constexpr int kPStride = kBN + 4;  // fp32 partial tile row stride (floats)
 
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PfArgs a)
 {
@@ -180,7 +205,10 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     const PfSeg &sg = a.seg[si];
     const int m0 = mt * kBM, n0 = (nt - sg.ntile0) * kBN;
     const int r = a.r;
-    const int ktiles = (a.Ktot + kBKp - 1) / kBKp;
+    const int ktiles_all = (a.Ktot + kBKp - 1) / kBKp;
+    const int kq = (int)blockIdx.z;
+    const int kt0 = kq * a.kts;
+    const int ktiles = min(ktiles_all, kt0 + a.kts);  // this CTA: k-tiles [kt0, ktiles)
     const int vt_bytes = a.rpad * 128;
 
     // shared memory: stages | barriers | tmem holder | s tile
@@ -229,7 +257,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
         if (lane == 0) {
             int s = 0;
             unsigned ph = 0;
-            for (int kt = 0; kt < ktiles; ++kt) {
+            for (int kt = kt0; kt < ktiles; ++kt) {
                 if (!pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty)) {
                     abort_flag = 1;
                     break;
@@ -238,7 +266,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 pf_expect_tx(&full[s], kATile + kBTile);
                 const int kc = kt * kBKp;
                 pf_tma_2d(st, &a.mapa, kc, m0, &full[s]);
-                pf_tma_2d(st + kATile, &sg.mapb, kc % a.in, n0, &full[s]);
+                pf_tma_2d(st + kATile, &sg.mapb, kc % a.kmod, n0, &full[s]);
                 if (++s == a.nst) {
                     s = 0;
                     ph ^= 1u;
@@ -253,7 +281,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             int s = 0;
             unsigned ph = 0;
             bool ok = true;
-            for (int kt = 0; kt < ktiles; ++kt) {
+            for (int kt = kt0; kt < ktiles; ++kt) {
                 if (!pf_wait(&full[s], ph, a.status, kWaitRingFull)) {
                     ok = false;
                     abort_flag = 1;
@@ -265,7 +293,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 #pragma unroll
                 for (int k = 0; k < kBKp / 16; ++k) {
                     const uint64_t da = sdesc(sa + 32 * k);
-                    const uint32_t accum = (kt > 0 || k > 0) ? 1u : 0u;
+                    const uint32_t accum = (kt > kt0 || k > 0) ? 1u : 0u;
                     umma(t_main, da, sdesc(sb + 32 * k), id_main, accum);
                     if (r > 0) umma(t_aux, da, sdesc(sv + 32 * k), id_z, accum);
                 }
@@ -300,7 +328,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             int s = 0;
             unsigned ph = 0;
             const int nch = (a.rpad < r ? a.rpad : r) * 8;  // (row j, 8-column chunk c) pairs, j < r
-            for (int kt = 0; kt < ktiles; ++kt) {
+            for (int kt = kt0; kt < ktiles; ++kt) {
                 int ok = 1;
                 if (et == 0) ok = pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty);
                 if (et == 0 && !ok) abort_flag = 1;
@@ -313,8 +341,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     float v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int kglob = kb + 8 * c + e;  // position along Ktot; V row kglob mod in
-                        v[e] = kglob < a.Ktot ? bf2f(sg.V[(int64_t)(kglob % a.in) * r + j]) : 0.f;
+                        const int kglob = kb + 8 * c + e;  // position along Ktot
+                        const int krow = kglob % a.kmod;   // V row
+                        v[e] = (kglob < a.Ktot && krow < a.in) ? bf2f(sg.V[(int64_t)krow * r + j]) : 0.f;
                     }
                     uint4 pk = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
                                           pack_bf16(v[6], v[7]));
@@ -417,6 +446,13 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                 float yv[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) yv[i] = fmaf(s_tile[c + i], acc[i], dl[i]);
+                if (a.ns > 1) {  // partial over this K split: to shared memory, added across the cluster below
+                    float *prow = reinterpret_cast<float *>(smem) + erow * kPStride + c;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<float4 *>(prow)[q] = make_float4(yv[4 * q], yv[4 * q + 1], yv[4 * q + 2], yv[4 * q + 3]);
+                    continue;
+                }
                 const int nvalid = sg.out - (n0 + c);
                 char *dst = static_cast<char *>(sg.y) + ((int64_t)m * sg.out + n0 + c) * es;
                 const bool vec = nvalid >= 16 && ((reinterpret_cast<uintptr_t>(dst) & 15) == 0);
@@ -446,6 +482,38 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
     }
     tc_fence_before();
     __syncthreads();
+    if (a.ns > 1) {
+        // Deterministic sum of the ns K-split partials (rank order), rows of
+        // the tile shared out among the cluster's CTAs, then the cast.
+        pf_cluster_sync();
+        const uint32_t me = cluster_rank();
+        const int rlo = (int)(me * kBM / a.ns), rhi = (int)((me + 1) * kBM / a.ns);
+        const float *pt = reinterpret_cast<const float *>(smem);
+        const int es = a.ydt == WL_OUT_F32 ? 4 : 2;
+        for (int idx = threadIdx.x; idx < (rhi - rlo) * (kBN / 4); idx += kPfThreads) {
+            const int row = rlo + idx / (kBN / 4), col = 4 * (idx % (kBN / 4));
+            const int m = m0 + row;
+            if (m >= a.T || n0 + col >= sg.out) continue;
+            float4 sum = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int p = 0; p < a.ns; ++p) {
+                const float4 v = ld_peer4(pt + row * kPStride + col, (uint32_t)p);
+                sum.x += v.x;
+                sum.y += v.y;
+                sum.z += v.z;
+                sum.w += v.w;
+            }
+            const float yv[4] = {sum.x, sum.y, sum.z, sum.w};
+            const int nvalid = sg.out - (n0 + col);
+            char *dst = static_cast<char *>(sg.y) + ((int64_t)m * sg.out + n0 + col) * es;
+            for (int i = 0; i < 4 && i < nvalid; ++i) {
+                if (a.ydt == WL_OUT_F32)
+                    reinterpret_cast<float *>(dst)[i] = yv[i];
+                else
+                    reinterpret_cast<bf16 *>(dst)[i] = __float2bfloat16_rn(yv[i]);
+            }
+        }
+        pf_cluster_sync();  // peers are done reading this CTA's partial tile
+    }
     if (warp == 1) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols));
@@ -457,19 +525,20 @@ static std::mutex g_pf_mu;
 static std::unordered_map<int, int> g_pf_attr;
 
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
-                         int64_t in, int64_t Ktot, int64_t r, int ydt, cudaStream_t st)
+                         int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st)
 {
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
     if (!di) return s;
     if (r > 128) return fail(WL_ERR_UNSUPPORTED, "prefill: r > 128");
-    if (Ktot != in && (Ktot != 2 * in || in % kBKp != 0))
-        return fail(WL_ERR_UNSUPPORTED, "prefill: hi/lo input needs in %% 64 == 0");
+    if (kmod < in || (Ktot > kmod && kmod % kBKp != 0))
+        return fail(WL_ERR_UNSUPPORTED, "prefill: bad K period");
     PfArgs a = {};
     a.nseg = nproj;
     a.T = (int)T;
     a.in = (int)in;
     a.Ktot = (int)Ktot;
+    a.kmod = (int)kmod;
     a.r = (int)r;
     a.ydt = ydt;
     a.rpad = r > 0 ? (int)((r + 15) / 16 * 16) : 0;
@@ -511,11 +580,103 @@ wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *co
             g_pf_attr[di->device] = 1;
         }
     }
-    const dim3 grid((unsigned)((T + kBM - 1) / kBM), (unsigned)ntile);
-    prefill_kernel<<<grid, kPfThreads, smem, st>>>(a);
-    cudaError_t e = cudaGetLastError();
+    // K splits: enough CTAs for the SMs, and (fp32 outputs) at most 4096 k
+    // per accumulation chain: the tensor cores' fp32 accumulation error grows
+    // with the length of the chain, and the splits meet in exact fp32.
+    const int mtiles = (int)((T + kBM - 1) / kBM);
+    const int ktiles = (int)((Ktot + kBKp - 1) / kBKp);
+    const int ctas = mtiles * ntile;
+    int ns = di->sm_count / ctas;
+    if (ydt == WL_OUT_F32) {
+        const int need = (ktiles + 63) / 64;
+        if (ns < need) ns = need;
+    }
+    if (ns > 8) ns = 8;
+    if (ns > ktiles / 4) ns = ktiles / 4;
+    if (ns < 1) ns = 1;
+    a.kts = (ktiles + ns - 1) / ns;
+    a.ns = (ktiles + a.kts - 1) / a.kts;
+    if (a.ns > 1 && nst * a.stage_bytes < kBM * kPStride * 4)
+        return fail(WL_ERR_UNSUPPORTED, "prefill: no room for the split-K partial tile");
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)mtiles, (unsigned)ntile, (unsigned)a.ns);
+    cfg.blockDim = dim3(kPfThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = (unsigned)a.ns;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    void *args[] = {&a};
+    cudaError_t e = cudaLaunchKernelExC(&cfg, (const void *)prefill_kernel, args);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return WL_OK;
+}
+
+// h = gelu_tanh(g) * u as bf16 into hb[t*ld + j]; with lo_off > 0 also the
+// rounding remainder (h - bf16(h)) as bf16 at column lo_off + j.  Columns
+// [inter, kmod) of each part are zeroed (they meet zero-filled W0 columns, but
+// garbage there could be NaN).
+__global__ void mlp_gelu_kernel(const float *__restrict__ g, const float *__restrict__ u, bf16 *hb, int64_t T,
+                                int inter, int kmod, int ld, int lo_off)
+{
+    const int64_t n = T * (int64_t)kmod;
+    for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n; idx += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t t = idx / kmod;
+        const int j = (int)(idx - t * kmod);
+        float hv = 0.f;
+        if (j < inter) {
+            const float gv = g[t * inter + j], uv = u[t * inter + j];
+            const float c = 0.7978845608028654f;  // sqrt(2/pi)
+            hv = 0.5f * gv * (1.0f + tanhf(c * (gv + 0.044715f * gv * gv * gv))) * uv;
+        }
+        const bf16 hi = __float2bfloat16_rn(hv);
+        hb[t * ld + j] = hi;
+        if (lo_off > 0) hb[t * ld + lo_off + j] = __float2bfloat16_rn(hv - __bfloat162float(hi));
+    }
+}
+
+static inline int64_t al256(int64_t v) { return (v + 255) / 256 * 256; }
+
+size_t prefill_mlp_workspace_bytes(int64_t T, int64_t inter, int ydt)
+{
+    const int64_t kmod = (inter + kBKp - 1) / kBKp * kBKp;
+    const int64_t ld = ydt == WL_OUT_F32 ? 2 * kmod : kmod;
+    return (size_t)(256 + 2 * al256(T * inter * 4) + al256(T * ld * 2));
+}
+
+wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up, const wl_proj &down,
+                             void *y, int64_t T, int64_t hidden, int64_t inter, int64_t r, void *ws,
+                             size_t ws_bytes, int ydt, cudaStream_t st)
+{
+    if (ws_bytes < prefill_mlp_workspace_bytes(T, inter, ydt))
+        return fail(WL_ERR_WORKSPACE, "MLP workspace too small for %lld tokens", (long long)T);
+    char *w = static_cast<char *>(ws);
+    float *g = reinterpret_cast<float *>(w + 256);
+    float *u = reinterpret_cast<float *>(w + 256 + al256(T * inter * 4));
+    bf16 *hb = reinterpret_cast<bf16 *>(w + 256 + 2 * al256(T * inter * 4));
+    const int64_t kmod = (inter + kBKp - 1) / kBKp * kBKp;
+    const int64_t ld = ydt == WL_OUT_F32 ? 2 * kmod : kmod;
+    // gate and up: one launch, x read once, fp32 results
+    const wl_proj gu[2] = {gate, up};
+    void *ys[2] = {g, u};
+    wl_status s = launch_prefill(x, gu, 2, ys, T, hidden, hidden, hidden, r, WL_OUT_F32, st);
+    if (s != WL_OK) return s;
+    const DeviceInfo *di = device_info(&s);
+    if (!di) return s;
+    const int64_t n = T * kmod;
+    int blocks = (int)((n + 255) / 256);
+    if (blocks > di->sm_count * 16) blocks = di->sm_count * 16;
+    mlp_gelu_kernel<<<blocks, 256, 0, st>>>(g, u, hb, T, (int)inter, (int)kmod, (int)ld,
+                                           ydt == WL_OUT_F32 ? (int)kmod : 0);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "MLP activation launch");
+    // down: K walks [h_hi | h_lo] (or h_hi only for bf16 outputs)
+    void *yd[1] = {y};
+    return launch_prefill(hb, &down, 1, yd, T, inter, ld, kmod, r, ydt, st);
 }
 
 }  // namespace wl

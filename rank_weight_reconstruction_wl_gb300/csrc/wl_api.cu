@@ -90,6 +90,9 @@ static constexpr int64_t kMaxDim = (int64_t)1 << 30;
 // Token counts up to this run the HBM-streaming decode kernels; larger ones
 // run the tensor-core prefill kernel.
 static constexpr int64_t kDecodeMaxTokens = 64;
+// The fused MLP's streaming kernels take up to 8 tokens per pass; more tokens
+// go to the tensor-core path (gate and up in one launch, then down).
+static constexpr int64_t kMlpDecodeMaxTokens = 8;
 
 static wl_status check_dims(int64_t T, int64_t in, int64_t out, int64_t r)
 {
@@ -152,7 +155,7 @@ wl_status wl_linear(const void *x, const void *W0, const float *s, const void *U
     wl_proj p = {W0, s, U, V, out};
     void *ys[1] = {y};
     if (T > kDecodeMaxTokens)
-        return launch_prefill(static_cast<const bf16 *>(x), &p, 1, ys, T, in, in, r, ydt,
+        return launch_prefill(static_cast<const bf16 *>(x), &p, 1, ys, T, in, in, in, r, ydt,
                               static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), &p, 1, ys, T, in, r, ydt,
                                 static_cast<cudaStream_t>(stream));
@@ -172,7 +175,7 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
     }
     WL_TRY(begin());
     if (T > kDecodeMaxTokens)
-        return launch_prefill(static_cast<const bf16 *>(x), ps, 3, ys, T, in, in, r, ydt,
+        return launch_prefill(static_cast<const bf16 *>(x), ps, 3, ys, T, in, in, in, r, ydt,
                               static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), ps, 3, ys, T, in, r, ydt,
                                 static_cast<cudaStream_t>(stream));
@@ -183,8 +186,10 @@ size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t 
     if (T < 1 || hidden < 8 || inter < 8 || hidden % 8 || inter % 8 || r < 0 || r > WL_MAX_RANK ||
         hidden > kMaxDim || inter > kMaxDim || T > kMaxDim)
         return 0;
-    (void)ydt;
-    return decode_mlp_workspace_bytes(hidden, inter, r);
+    const size_t dec = decode_mlp_workspace_bytes(hidden, inter, r);
+    if (T <= kMlpDecodeMaxTokens) return dec;
+    const size_t pre = prefill_mlp_workspace_bytes(T, inter, ydt);
+    return pre > dec ? pre : dec;
 }
 
 wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj down, void *y,
@@ -208,6 +213,9 @@ wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj do
     if (ws_bytes < need)
         return fail(WL_ERR_WORKSPACE, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
     WL_TRY(begin());
+    if (T > kMlpDecodeMaxTokens)
+        return launch_prefill_mlp(static_cast<const bf16 *>(x), gate, up, down, y, T, hidden, inter, r,
+                                  workspace, ws_bytes, ydt, static_cast<cudaStream_t>(stream));
     return launch_decode_mlp(static_cast<const bf16 *>(x), gate, up, down, y, T, hidden, inter, r,
                              workspace, ws_bytes, ydt, static_cast<cudaStream_t>(stream));
 }

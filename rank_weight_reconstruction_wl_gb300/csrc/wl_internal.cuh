@@ -93,10 +93,15 @@ wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &u
                             int64_t inter, int64_t r, void *ws, size_t ws_bytes,
                             int ydt, cudaStream_t st);
 size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r);
-// Tensor-core path for large T.  x is [T, Ktot] with Ktot = in, or 2*in when
-// x holds bf16 hi and lo parts of each row side by side (in % 64 == 0).
+// Tensor-core path for large T.  x is [T, Ktot]; K position k meets W0
+// column and V row k % kmod (zero where that is >= in), so x may hold several
+// parts of each row side by side (bf16 hi and lo parts: Ktot = 2*kmod).
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
-                         int64_t in, int64_t Ktot, int64_t r, int ydt, cudaStream_t st);
+                         int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st);
+size_t prefill_mlp_workspace_bytes(int64_t T, int64_t inter, int ydt);
+wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up, const wl_proj &down,
+                             void *y, int64_t T, int64_t hidden, int64_t inter, int64_t r, void *ws,
+                             size_t ws_bytes, int ydt, cudaStream_t st);
 wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U,
                              const bf16 *V, void *W_eff, int64_t out, int64_t in,
                              int64_t r, int dt, cudaStream_t st);

@@ -72,3 +72,35 @@ def test_prefill_matches_decode_rows(wl, gpu):
         yd = _run(wl, x[t0:t0 + 8], th, torch.float32, gpu).cpu()
         d = (yd - yp[t0:t0 + 8]).abs().max().item()
         assert d <= 1e-5 * yp.abs().max().item()
+
+
+def _mlp_case(seed, T, hidden, inter, r):
+    g = wl_synth.make_generator(seed)
+    x = wl_synth.draw_x(g, T, hidden)
+    ths = [wl_synth.draw_theta(g, hidden, inter, r), wl_synth.draw_theta(g, hidden, inter, r),
+           wl_synth.draw_theta(g, inter, hidden, r)]
+    return x, ths
+
+
+@pytest.mark.parametrize("T", [9, 65, 200])
+@pytest.mark.parametrize("hidden,inter,r", [(64, 136, 3), (264, 520, 0), (128, 1000, 33)])
+def test_prefill_mlp_small(wl, orc, gpu, T, hidden, inter, r):
+    x, ths = _mlp_case(T * 7 + r, T, hidden, inter, r)
+    ref = orc.mlp_geglu(x, *ths)
+    for ydt in YDT:
+        buf, y, pad = guarded_empty((T, hidden), ydt, gpu)
+        wl.wl_mlp_geglu_fused(x.to(gpu), *[t.to(gpu) for t in ths], y=y, ydt=ydt)
+        assert wl.wl_device_status() == wl.WL_OK, wl.wl_last_error()
+        assert_canaries(buf, pad)
+        assert_parity(y, ref, ydt, f"mlp T={T}")
+
+
+@pytest.mark.parametrize("r", [16, 32])
+def test_prefill_mlp_gemma_T2048_sampled(wl, orc, gpu, r):
+    x, ths = _mlp_case(r, 2048, 1152, 6912, r)
+    tok = np.sort(np.random.default_rng(r).choice(2048, 48, replace=False))
+    ref = orc.mlp_geglu(x, *ths, tok=tok)
+    for ydt in YDT:
+        y = wl.wl_mlp_geglu_fused(x.to(gpu), *[t.to(gpu) for t in ths], ydt=ydt)
+        assert wl.wl_device_status() == wl.WL_OK
+        assert_parity(y[torch.as_tensor(tok, device=gpu)], ref, ydt, "mlp T=2048")
