@@ -87,9 +87,18 @@ class Clocks:
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                 "-lms", "25"], stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        # nvidia-smi takes a moment to start: wait for its first sample (taken
+        # before the timed region, and dropped in stop()) so that the samples
+        # kept all fall inside the region
+        t0 = time.time()
+        while time.time() - t0 < 5.0 and self.proc.poll() is None:
+            if os.path.getsize(self.f.name) > 0:
+                break
+            time.sleep(0.01)
 
     def stop(self):
         if self.proc is None:
@@ -101,7 +110,7 @@ class Clocks:
             self.proc.kill()
         self.f.flush()
         self.f.seek(0)
-        rows = [ln.split(",") for ln in self.f.read().strip().splitlines() if ln.strip()]
+        rows = [ln.split(",") for ln in self.f.read().strip().splitlines() if ln.strip()][1:]
         os.unlink(self.f.name)
         sm, smax, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -323,12 +332,86 @@ def run_wl(args):
         }
         if ck is not None:
             line["clocks"] = ck
+        if not args.no_prefill:
+            line["prefill_T2048"] = measure_prefill(dev)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = time_oracle_sample(r)
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
+    """TFLOP/s of the Gemma-1B layer at prefill (T tokens): fused QKV, O and
+    the fused MLP on the tensor-core path, rotating over `nlayers` distinct
+    weight sets (216 MB at r=16, larger than L2)."""
+    import torch
+    import rank_weight_reconstruction_wl_gb300 as wl
+    from rank_weight_reconstruction_wl_gb300.stack import build_layers
+
+    layers = build_layers(nlayers, nlayers, T, SHAPES, r, seed=7, device=dev)
+    g = torch.Generator(device=dev)
+    g.manual_seed(3)
+    z = dict(dtype=torch.bfloat16, device=dev)
+    x = torch.randn(T, SHAPES["hidden"], generator=g, device=dev).to(torch.bfloat16)
+    yq = torch.empty(T, SHAPES["q"], **z)
+    yk = torch.empty(T, SHAPES["kv"], **z)
+    yv = torch.empty(T, SHAPES["kv"], **z)
+    yo = torch.empty(T, SHAPES["hidden"], **z)
+    ym = torch.empty(T, SHAPES["hidden"], **z)
+    ws = wl.mlp_workspace(T, SHAPES["hidden"], SHAPES["inter"], r, torch.bfloat16, dev)
+    st = torch.cuda.Stream(dev)
+    ev = {k: [] for k in ("qkv", "o", "mlp")}
+
+    def layer(th, timed):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        if timed:
+            e[0].record(st)
+        wl.wl_qkv_fused(x, th.q, th.k, th.v, outs=(yq, yk, yv), stream=st)
+        if timed:
+            e[1].record(st)
+        wl.wl_linear(yq, th.o.W0, th.o.s, th.o.U, th.o.V, y=yo, stream=st)
+        if timed:
+            e[2].record(st)
+        wl.wl_mlp_geglu_fused(yo, th.gate, th.up, th.down, y=ym, workspace=ws, stream=st)
+        if timed:
+            e[3].record(st)
+            ev["qkv"].append((e[0], e[1]))
+            ev["o"].append((e[1], e[2]))
+            ev["mlp"].append((e[2], e[3]))
+
+    with torch.cuda.stream(st):
+        for th in layers:
+            layer(th, False)
+        st.synchronize()
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(st)
+        for _ in range(reps):
+            for th in layers:
+                layer(th, False)
+        t1.record(st)
+        st.synchronize()
+        for th in layers:
+            layer(th, True)
+        st.synchronize()
+    ms = t0.elapsed_time(t1) / (reps * nlayers)
+    flops = layer_flops(SHAPES, T, r)
+    h, q, kv, i = SHAPES["hidden"], SHAPES["q"], SHAPES["kv"], SHAPES["inter"]
+    part_flops = {"qkv": 2 * T * (h * (q + 2 * kv) + r * 3 * h + r * (q + 2 * kv)),
+                  "o": 2 * T * (q * h + r * (q + h)),
+                  "mlp": 2 * T * (3 * h * i + r * 3 * (h + i))}
+    parts = {}
+    for k, pairs in ev.items():
+        pms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
+        parts[k] = {"us": round(pms * 1e3, 2), "tflops": round(part_flops[k] / (pms * 1e-3) / 1e12, 1)}
+    _, bf16_peak, kind = load_peaks()
+    tf = flops / (ms * 1e-3) / 1e12
+    return {"T": T, "r": r, "ms_per_layer": round(ms, 4), "tflops": round(tf, 1),
+            "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_tflops": bf16_peak, "peak_kind": kind,
+            "layer_gflop": round(flops / 1e9, 2), "parts": parts,
+            "l2": f"{nlayers} weight sets rotated (larger than L2)"}
 
 
 def load_traffic():
@@ -346,11 +429,12 @@ def load_traffic():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="wl", choices=["wl", "reference"])
     ap.add_argument("--rank", type=int, default=4, help="LoRA rank r of the theta bundles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true", help="skip the T=2048 prefill measurement")
     ap.add_argument("--layers", type=int, default=L_LAYERS,
                     help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()

@@ -53,7 +53,11 @@ class DecoderStack:
         self.stream = torch.cuda.Stream(self.dev)
         self.graph = None
         self.use_graph = use_graph
-        self.launches_per_step = 3 * len(layers) * ((T + 7) // 8 if T <= 64 else 1)
+        # kernels per layer: fused QKV 1, O 1; the MLP is 2 (gate/up, down) on the
+        # decode path (T <= 8) and 3 (gate/up, GELU, down) on the prefill path
+        lin = (T + 63) // 64 if T <= 64 else 1
+        mlp = 2 if T <= 8 else 3
+        self.launches_per_step = len(layers) * (2 * lin + mlp)
 
     @property
     def out(self) -> torch.Tensor:
