@@ -151,6 +151,69 @@ wl_status wl_materialize(const void *W0, const float *s, const void *U, const vo
                          wl_out_dtype dt, void *stream);
 
 /*
+ * Decoder-layer stacks at decode size, in one launch per step.
+ *
+ * A weightless decoder layer applies its projections in a chain ("Serve and
+ * generate with weightless": every linear layer of the model is a theta
+ * bundle; "In-kernel reconstruction", formula section, per projection):
+ *     q, k, v = wl(x_l; q), wl(x_l; k), wl(x_l; v)
+ *     o       = wl(q; o)                  (q stands in for attention, which
+ *                                          is not part of the method)
+ *     g, u    = wl(o; gate), wl(o; up);   h = gelu_tanh(g) * u
+ *     x_{l+1} = wl(h; down)
+ * Every output is bf16 (round-to-nearest-even of the fp32 result, as for
+ * wl_linear with WL_OUT_BF16); h stays fp32 inside the launch, as in
+ * wl_mlp_geglu_fused.  Each output of each layer equals, within fp32
+ * accumulation order, the single-projection calls on that layer's bf16
+ * inputs.  At batch 1 a launch per projection costs more than its weight
+ * traffic ("What weightless inference costs": at batch-1 decode extra
+ * dispatches, not extra arithmetic, dominate), so one launch streams the
+ * weights of all L layers and follows the data dependencies inside it.
+ */
+typedef struct {
+    wl_proj q, k, v, o, gate, up, down; /* gate.out == up.out == inter, o.out == down.out == hidden */
+} wl_layer;
+
+/* Output buffers of one layer, bf16 [T, n], row-major, 16-byte aligned. */
+typedef struct {
+    void *yq; /* [T, q.out]  */
+    void *yk; /* [T, k.out]  */
+    void *yv; /* [T, v.out]  */
+    void *yo; /* [T, hidden] */
+    void *ym; /* [T, hidden]: the layer's output and the next layer's input */
+} wl_layer_out;
+
+typedef struct wl_stack_s *wl_stack;
+
+/*
+ * wl_stack_create -- bind L layers and their output buffers (all device
+ * memory owned by the caller, which must outlive the stack) into a stack for
+ * T tokens on the current device.  Allocates the stack's own device tables
+ * and scratch (cudaMalloc; freed by wl_stack_destroy) and uploads them
+ * synchronously: call it outside stream capture.
+ * Limits: 1 <= T <= 4, 0 <= r <= 32; hidden, q.out and gate.out multiples of
+ * 64; every layer with the shapes of layer 0; W0 and V 16-byte aligned.
+ * Output buffers of different layers must be distinct and may not alias any
+ * input.  Sizes outside these limits give WL_ERR_UNSUPPORTED (use the
+ * per-projection calls).  On error *out is NULL.
+ */
+wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, const wl_layer_out *outs,
+                          int64_t L, int64_t T, int64_t hidden, int64_t r);
+
+/*
+ * wl_stack_decode -- one pass over all layers of the stack for input x
+ * [T, hidden] bf16 (device, 16-byte aligned), asynchronous on `stream`.
+ * Writes every output of every layer.  Launches must not overlap: calls on
+ * one stream never do.  The launch is cooperative (one CTA per SM); it
+ * cannot be captured into a CUDA graph on drivers that refuse cooperative
+ * launches in capture.
+ */
+wl_status wl_stack_decode(wl_stack stack, const void *x, void *stream);
+
+/* Free the stack's device memory (after its last launch has completed). */
+void wl_stack_destroy(wl_stack stack);
+
+/*
  * wl_band_of_layer -- which of the G shared W0 blocks layer `layer` of an
  * L-layer stack uses: floor(layer * G / L) (contiguous bands).  G = L is the
  * passthrough point (one W0 per layer, "Set the fast path on NVIDIA"); G = 1

@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "WLError", "lib", "library_path", "wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes",
     "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status",
-    "wl_last_error", "wl_version", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
+    "wl_last_error", "wl_version", "WLStack", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
     "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
 ]
 
@@ -38,8 +38,8 @@ STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3:
 
 # Every function include/wl.h declares.
 EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
-                    "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status", "wl_last_error",
-                    "wl_version")
+                    "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_stack_create", "wl_stack_decode",
+                    "wl_stack_destroy", "wl_band_of_layer", "wl_device_status", "wl_last_error", "wl_version")
 
 
 class WLError(RuntimeError):
@@ -51,6 +51,14 @@ class WLError(RuntimeError):
 class _Proj(C.Structure):
     _fields_ = [("W0", C.c_void_p), ("s", C.c_void_p), ("U", C.c_void_p), ("V", C.c_void_p),
                 ("out", C.c_int64)]
+
+
+class _Layer(C.Structure):
+    _fields_ = [(n, _Proj) for n in ("q", "k", "v", "o", "gate", "up", "down")]
+
+
+class _LayerOut(C.Structure):
+    _fields_ = [(n, C.c_void_p) for n in ("yq", "yk", "yv", "yo", "ym")]
 
 
 _lock = threading.Lock()
@@ -87,6 +95,13 @@ def lib():
         L.wl_mlp_geglu_fused_noalloc.restype = st
         L.wl_materialize.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, C.c_int, vp]
         L.wl_materialize.restype = st
+        L.wl_stack_create.argtypes = [C.POINTER(C.c_void_p), C.POINTER(_Layer), C.POINTER(_LayerOut),
+                                      i64, i64, i64, i64]
+        L.wl_stack_create.restype = st
+        L.wl_stack_decode.argtypes = [vp, vp, vp]
+        L.wl_stack_decode.restype = st
+        L.wl_stack_destroy.argtypes = [vp]
+        L.wl_stack_destroy.restype = None
         L.wl_band_of_layer.argtypes = [i64, i64, i64]
         L.wl_band_of_layer.restype = i64
         L.wl_device_status.argtypes = [vp]
@@ -277,6 +292,73 @@ def wl_materialize(W0, s, U, V, dt=torch.bfloat16, out=None, stream=None):
         _check(lib().wl_materialize(p.W0, p.s, p.U, p.V, _ptr(out), o, inp, r, code,
                                     _stream(stream, W0.device)))
     return out
+
+
+class WLStack:
+    """A stack of weightless decoder layers run by one launch per step
+    (wl_stack_create / wl_stack_decode).
+
+    layers: objects with q, k, v, o, gate, up, down theta bundles (all bf16
+    W0, U, V and fp32 s on one device).  The stack owns one set of bf16 output
+    buffers per layer, ``outs[l] = {"yq", "yk", "yv", "yo", "ym"}``;
+    ``decode(x)`` writes all of them and returns ``outs[-1]["ym"]``.
+    Raises WLError (WL_ERR_UNSUPPORTED) for sizes the stack kernel does not
+    take (T > 4, r > 32, hidden / q.out / gate.out not multiples of 64).
+    """
+
+    def __init__(self, layers, T: int, device=None):
+        self.dev = torch.device(device) if device is not None else layers[0].q.W0.device
+        self.T = int(T)
+        th0 = layers[0]
+        self.hidden = int(th0.q.W0.shape[1])
+        self.r = _rank(th0.q)
+        qd, kd, vd = th0.q.W0.shape[0], th0.k.W0.shape[0], th0.v.W0.shape[0]
+        inter = th0.gate.W0.shape[0]
+        h, r = self.hidden, self.r
+        L = len(layers)
+        z = dict(dtype=torch.bfloat16, device=self.dev)
+        self.outs = [{"yq": torch.empty(T, qd, **z), "yk": torch.empty(T, kd, **z),
+                      "yv": torch.empty(T, vd, **z), "yo": torch.empty(T, h, **z),
+                      "ym": torch.empty(T, h, **z)} for _ in range(L)]
+        self._layers = (_Layer * L)()
+        self._louts = (_LayerOut * L)()
+        self._keep = layers  # the stack refers to the layers' device memory
+        for l, th in enumerate(layers):
+            ly = self._layers[l]
+            ly.q = _proj(th.q, h, r, f"layer {l} q")
+            ly.k = _proj(th.k, h, r, f"layer {l} k")
+            ly.v = _proj(th.v, h, r, f"layer {l} v")
+            ly.o = _proj(th.o, qd, r, f"layer {l} o")
+            ly.gate = _proj(th.gate, h, r, f"layer {l} gate")
+            ly.up = _proj(th.up, h, r, f"layer {l} up")
+            ly.down = _proj(th.down, inter, r, f"layer {l} down")
+            o = self.outs[l]
+            self._louts[l] = _LayerOut(o["yq"].data_ptr(), o["yk"].data_ptr(), o["yv"].data_ptr(),
+                                       o["yo"].data_ptr(), o["ym"].data_ptr())
+        self._h = C.c_void_p()
+        with torch.cuda.device(self.dev):
+            _check(lib().wl_stack_create(C.byref(self._h), self._layers, self._louts, L, self.T, h, r))
+
+    @property
+    def out(self) -> torch.Tensor:
+        return self.outs[-1]["ym"]
+
+    def decode(self, x: torch.Tensor, stream=None) -> torch.Tensor:
+        _need(x, "x", torch.bfloat16, (self.T, self.hidden))
+        with torch.cuda.device(self.dev):
+            _check(lib().wl_stack_decode(self._h, _ptr(x), _stream(stream, self.dev)))
+        return self.out
+
+    def close(self):
+        if self._h:
+            lib().wl_stack_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def wl_band_of_layer(layer: int, L: int, G: int) -> int:

@@ -10,7 +10,10 @@
 //   * z = x V is formed in the same K loop by a second MMA of the same x
 //     tile against V^T (N = r rounded up to 16) into TMEM columns [256, ...);
 //     V^T is written into swizzled shared memory by the epilogue warps while
-//     the main loop runs (V is [in, r], so its transpose is not a TMA tile);
+//     the main loop runs (V is [in, r], so its transpose is not a TMA tile):
+//     the stage's 64 V rows arrive by bulk copy with the x and W0 tiles and
+//     are transposed shared-to-shared, or (r not a multiple of 8) are read
+//     from global memory;
 //   * the epilogue splits z into bf16 hi + lo parts (z = hi + lo to about 16
 //     bits) and runs the rank-r delta [hi | lo] [U | U]^T as one more MMA into
 //     TMEM columns [256, 512), then forms s * acc + delta in fp32 and casts
@@ -83,6 +86,16 @@ __device__ __forceinline__ void pf_tma_2d(void *dst, const CUtensorMap *map, int
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(s32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(s32(bar))
         : "memory");
+}
+
+// Contiguous global -> shared copy (16-byte aligned addresses, size a
+// multiple of 16) completing on `bar`'s transaction count.
+__device__ __forceinline__ void pf_bulk(void *dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     s32(dst)),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(s32(bar))
+                 : "memory");
 }
 
 // Shared-memory matrix descriptor: K-major operand, 128-byte swizzle, rows of
@@ -188,7 +201,8 @@ struct PfArgs {
     CUtensorMap mapa;  // x [T, Ktot], box 64 x 128
     int nseg;
     int T, in, Ktot, kmod, r, ydt;  // K position k maps to W0 column / V row k % kmod (< in)
-    int rpad, Kz, nst, stage_bytes, full_count;
+    int rpad, Kz, nst, stage_bytes;
+    int vstage;  // 1: V rows arrive by bulk copy with the stage (r % 8 == 0, V 16-byte aligned)
     int ns, kts;  // K splits (= cluster size along z) and k-tiles per split
     unsigned *status;
 };
@@ -213,16 +227,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 
     // shared memory: stages | barriers | tmem holder | s tile
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + (size_t)a.nst * a.stage_bytes);
-    uint64_t *full = bars, *empty = bars + a.nst;
-    uint64_t *acc_full = bars + 2 * a.nst, *z_ready = acc_full + 1, *d_ready = acc_full + 2;
+    uint64_t *full = bars, *empty = bars + a.nst, *vfull = bars + 2 * a.nst;  // TMA done / V^T written / free
+    uint64_t *acc_full = bars + 3 * a.nst, *z_ready = acc_full + 1, *d_ready = acc_full + 2;
     uint32_t *tmem_hold = reinterpret_cast<uint32_t *>(acc_full + 3);
     volatile int &abort_flag = *reinterpret_cast<volatile int *>(tmem_hold + 1);
     float *s_tile = reinterpret_cast<float *>(tmem_hold + 4);
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.nst; ++i) {
-            pf_mbar_init(&full[i], a.full_count);
+            pf_mbar_init(&full[i], 1);
             pf_mbar_init(&empty[i], 1);
+            pf_mbar_init(&vfull[i], 1);
         }
         pf_mbar_init(acc_full, 1);
         pf_mbar_init(z_ready, 1);
@@ -263,10 +278,15 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
                     break;
                 }
                 char *st = smem + (size_t)s * a.stage_bytes;
-                pf_expect_tx(&full[s], kATile + kBTile);
                 const int kc = kt * kBKp;
+                const int krow0 = kc % a.kmod;  // V row of this stage's first K position
+                const int vrows = a.vstage ? max(0, min(kBKp, a.in - krow0)) : 0;
+                const unsigned vbytes = (unsigned)(vrows * r * 2);
+                pf_expect_tx(&full[s], kATile + kBTile + vbytes);
                 pf_tma_2d(st, &a.mapa, kc, m0, &full[s]);
-                pf_tma_2d(st + kATile, &sg.mapb, kc % a.kmod, n0, &full[s]);
+                pf_tma_2d(st + kATile, &sg.mapb, krow0, n0, &full[s]);
+                if (vbytes)
+                    pf_bulk(st + kATile + kBTile + vt_bytes, sg.V + (int64_t)krow0 * r, vbytes, &full[s]);
                 if (++s == a.nst) {
                     s = 0;
                     ph ^= 1u;
@@ -282,7 +302,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             unsigned ph = 0;
             bool ok = true;
             for (int kt = kt0; kt < ktiles; ++kt) {
-                if (!pf_wait(&full[s], ph, a.status, kWaitRingFull)) {
+                if (!pf_wait(&full[s], ph, a.status, kWaitRingFull) ||
+                    (r > 0 && !pf_wait(&vfull[s], ph, a.status, kWaitRingFull))) {
                     ok = false;
                     abort_flag = 1;
                     break;
@@ -329,29 +350,37 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             unsigned ph = 0;
             const int nch = (a.rpad < r ? a.rpad : r) * 8;  // (row j, 8-column chunk c) pairs, j < r
             for (int kt = kt0; kt < ktiles; ++kt) {
+                // staged: wait for the stage's copies (V rows included);
+                // otherwise only for the stage to be free
                 int ok = 1;
-                if (et == 0) ok = pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty);
+                if (et == 0)
+                    ok = a.vstage ? pf_wait(&full[s], ph, a.status, kWaitRingFull)
+                                  : pf_wait(&empty[s], ph ^ 1u, a.status, kWaitRingEmpty);
                 if (et == 0 && !ok) abort_flag = 1;
                 epi_sync();
                 if (abort_flag) break;
                 char *vt = smem + (size_t)s * a.stage_bytes + kATile + kBTile;
+                const bf16 *vst = reinterpret_cast<const bf16 *>(vt + vt_bytes);  // [64 rows][r]
                 const int kb = kt * kBKp;
+                const int krow0 = kb % a.kmod;
                 for (int idx = et; idx < nch; idx += 128) {
                     const int j = idx >> 3, c = idx & 7;
-                    float v[8];
+                    uint16_t v[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const int kglob = kb + 8 * c + e;  // position along Ktot
-                        const int krow = kglob % a.kmod;   // V row
-                        v[e] = (kglob < a.Ktot && krow < a.in) ? bf2f(sg.V[(int64_t)krow * r + j]) : 0.f;
+                        const int krow = krow0 + 8 * c + e;  // V row (a tile never crosses the K period)
+                        const bool in_range = kglob < a.Ktot && krow < a.in;
+                        const bf16 *src = a.vstage ? vst + (8 * c + e) * r + j : sg.V + (int64_t)krow * r + j;
+                        v[e] = in_range ? *reinterpret_cast<const uint16_t *>(src) : (uint16_t)0;
                     }
-                    uint4 pk = make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                                          pack_bf16(v[6], v[7]));
-                    *reinterpret_cast<uint4 *>(vt + swz(j, 8 * c, a.rpad)) = pk;
+                    *reinterpret_cast<uint4 *>(vt + swz(j, 8 * c, a.rpad)) =
+                        make_uint4(v[0] | (uint32_t)v[1] << 16, v[2] | (uint32_t)v[3] << 16,
+                                   v[4] | (uint32_t)v[5] << 16, v[6] | (uint32_t)v[7] << 16);
                 }
                 fence_async_smem();
                 epi_sync();
-                if (et == 0) pf_arrive(&full[s]);
+                if (et == 0) pf_arrive(&vfull[s]);
                 if (++s == a.nst) {
                     s = 0;
                     ph ^= 1u;
@@ -544,8 +573,12 @@ wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *co
     a.rpad = r > 0 ? (int)((r + 15) / 16 * 16) : 0;
     a.Kz = r > 0 ? (int)((2 * r + 63) / 64 * 64) : 0;
     a.status = di->status;
-    a.full_count = r > 0 ? 2 : 1;
-    a.stage_bytes = kATile + kBTile + a.rpad * 128;
+    // V rows by bulk copy: rows of r bf16 must be a whole number of 16-byte
+    // chunks, V 16-byte aligned, and the larger stage must still leave room
+    // for the epilogue's A_z / B_u tiles (checked below)
+    a.vstage = (r > 0 && r % 8 == 0 && (reinterpret_cast<uintptr_t>(proj[0].V) & 15) == 0) ? 1 : 0;
+    for (int j = 1; j < nproj; ++j)
+        if (reinterpret_cast<uintptr_t>(proj[j].V) & 15) a.vstage = 0;
     s = tmap_2d_bf16(x, Ktot, T, Ktot, kBKp, kBM, &a.mapa);
     if (s != WL_OK) return s;
     int ntile = 0;
@@ -562,12 +595,18 @@ wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *co
         ntile += (int)((proj[j].out + kBN - 1) / kBN);
     }
     // stages: as many as fit; the epilogue's A_z / B_u tiles reuse the stages
-    const int extra = 1024 + (2 * 8 + 3) * 8 + 16 + kBN * 4 + 64;
-    int nst = (di->max_smem_optin - extra) / a.stage_bytes;
-    if (nst > 4) nst = 4;
+    const int extra = 1024 + (3 * 8 + 3) * 8 + 16 + kBN * 4 + 64;
     const int need_epi = (a.Kz / 64) * (kATile + kBTile);
-    while (nst * a.stage_bytes < need_epi) ++nst;
-    if (nst < 2 || nst * a.stage_bytes + extra > di->max_smem_optin)
+    int nst = 0;
+    for (int pass = 0; pass < 2 && nst == 0; ++pass) {
+        if (pass == 1) a.vstage = 0;
+        a.stage_bytes = kATile + kBTile + a.rpad * 128 + (a.vstage ? kBKp * (int)r * 2 : 0);
+        int n = (di->max_smem_optin - extra) / a.stage_bytes;
+        if (n > 4) n = 4;
+        while (n * a.stage_bytes < need_epi) ++n;
+        if (n >= 2 && n * a.stage_bytes + extra <= di->max_smem_optin) nst = n;
+    }
+    if (nst == 0)
         return fail(WL_ERR_UNSUPPORTED, "prefill: r=%lld needs more shared memory than the device has", (long long)r);
     a.nst = nst;
     const int smem = nst * a.stage_bytes + extra;

@@ -1,0 +1,1115 @@
+// stack.cu -- a whole stack of weightless decoder layers at decode size
+// (T <= 4 tokens) in ONE persistent launch.
+//
+// Each layer runs four projection phases ("In-kernel reconstruction", formula
+// section, per projection):
+//     QKV  x_l  -> q, k, v          (three bundles sharing x_l)
+//     O    q    -> o                (q stands in for the attention output)
+//     GU   o    -> g, u;  h = gelu_tanh(g) * u
+//     D    h    -> x_{l+1}
+// At decode size the cost is streaming every W0 from HBM once; with one
+// launch per projection the fixed cost of each launch (start-up, the wait
+// for x behind the weight stream, the epilogue) dominates ("What weightless
+// inference costs": extra dispatches, not arithmetic, dominate at batch 1).
+// Here the weights of all layers form one stream that never waits for the
+// data dependencies between projections:
+//
+//   producer warp   walks the CTA's share of every phase in order and loads
+//                   each 64x64 W0 box (TMA, 128-byte swizzle) with the 64
+//                   matching rows of V into a ring of shared-memory stages,
+//                   waiting only for free stages;
+//   8 consumer warps  per phase: gather the phase input; then each warp takes
+//                   whole boxes (box j of the phase goes to warp j % 8) and
+//                   multiplies them on the tensor cores (mma.sync m16n8k16,
+//                   W0 rows as M, tokens as N), forming z = x V on the CUDA
+//                   cores; at the end of the phase the warps' sums are added
+//                   in warp order and p = s * acc + U z_range goes to a
+//                   global partial slot per (row tile, CTA).
+//
+// Work split.  A phase's boxes are numbered row tile by row tile (for GU a
+// row tile is a pair: the gate tile's boxes, then the up tile's) and the
+// phase's n CTAs take equal contiguous ranges: every CTA streams about the
+// same number of bytes.  A row tile is shared by the few CTAs whose ranges
+// touch it; each adds one partial (both terms of the projection are linear
+// in the K split).
+//
+// Publication without fences.  Every partial value is stored as one 64-bit
+// word holding the value and the launch's epoch.  A consumer polls the words
+// it needs until all carry the current epoch, then sums them in slot order
+// (every CTA sums in the same order, so all agree bit for bit) and rounds to
+// bf16 as the projection output is defined.  The CTA that owns box kb of the
+// phase's first row tile also stores input block kb to the previous phase's
+// output buffer, so every output element is written exactly once; k, v and
+// the last layer's output, which no phase reads, are stored by CTAs assigned
+// to them after their own work.  Slots and outputs are distinct per layer
+// and phase, so no write can overtake a read of an earlier layer, and the
+// epoch makes values left by an earlier launch invisible.
+//
+// The down projection takes h as two bf16 columns per token (h = hi + lo), so
+// its tensor-core product keeps fp32 accuracy; z uses hi + lo in fp32.
+//
+// Every wait (ring stages, partial words) is bounded; a wait that gives up
+// sets the status word and the CTA winds down after its copies in flight
+// land.  Co-residency of all CTAs (needed for the waits on other CTAs'
+// partials) is guaranteed by a cooperative launch of one CTA per SM.
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "dec_ptx.cuh"
+
+namespace wl {
+
+constexpr int kStThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
+constexpr int kStMaxT = 4;                 // tokens per launch
+constexpr int kStMaxR = 32;                // rank
+constexpr int kStBox = 64;                 // rows and columns of a W0 box
+constexpr int kStBoxBytes = kStBox * kStBox * 2;
+
+enum StKind { kQKV = 0, kO = 1, kGU = 2, kD = 3 };
+
+struct StSeg {
+    const CUtensorMap *map;  // W0 [out, K], box 64 x 64 (device memory)
+    const float *s;
+    const bf16 *U;
+    const bf16 *V;
+    bf16 *y;   // output [T, out] (bf16)
+    int out;
+    int rt0;   // first row tile of this segment within the phase
+    int nrt;   // row tiles
+};
+
+struct StPhase {
+    StSeg seg[3];
+    int nseg, kind;
+    int K, KB;     // input length and 64-wide k blocks
+    int nrt;       // row tiles (GU: gate/up pairs)
+    int bpr;       // boxes per row tile (GU: 2 * KB)
+    int nbox;      // nrt * bpr
+    int ncta;      // CTAs sharing the phase (<= grid, <= nbox: none has an empty range)
+    int nsub;      // parts per slot (GU: 2, gate and up)
+    int prev;      // phase producing the input, -1: the launch's x
+    bf16 *wy;      // the input vector's buffer (owner of box kb stores block kb), or null
+    int xw_ph, xw_rt0, xw_n;  // after its work, CTA c stores row tiles xw_rt0 + c (+ grid...) of phase xw_ph
+    const int *np;     // [nrt] partials per row tile
+    const int *slot0;  // [nrt] first slot of the row tile
+    unsigned long long *part;  // [slot][nsub][T][64] words: epoch << 32 | fp32 bits
+};
+
+// Phases per launch: the descriptors travel as a kernel parameter (read
+// through the constant cache; shared memory leaves little L1 for tables in
+// global memory), and the parameter space holds 24 layers.
+constexpr int kStMaxPh = 96;
+
+struct StArgs {
+    StPhase ph[kStMaxPh];
+    int nph;
+    const bf16 *x;  // [T, hidden] input of layer 0
+    int T, r, rr;   // rr: r rounded up to a power of two (<= 32)
+    unsigned epoch;
+    int nst;        // ring stages
+    int maxp;       // most pieces of one CTA in one phase
+    int xs32;       // x stage row stride (u32)
+    int us_bytes;   // bytes per piece in the U/s area
+    int wb_floats;  // floats per (piece, warp) partial block: [2T][64] sums, then [T][r] z
+    int wb_zoff;    // offset of the z part (2T * 64)
+    int maxnk;      // most input blocks one CTA stages in one phase
+    unsigned *status;
+};
+static_assert(sizeof(StPhase) <= 256, "phase descriptor grew");
+static_assert(sizeof(StArgs) <= 31 * 1024, "kernel parameter space");
+
+// ----------------------------------------------------------- small helpers
+// A phase's nbox boxes are shared by its first n CTAs: CTA c < n takes
+// [nbox*c/n, nbox*(c+1)/n) (at least one box, as n <= nbox); the others none.
+__device__ __forceinline__ int st_owner(int b, int nbox, int n)
+{
+    return (int)((((int64_t)b + 1) * n - 1) / nbox);
+}
+__device__ __forceinline__ int st_lo(int nbox, int c, int n)
+{
+    return (int)((int64_t)nbox * (c < n ? c : n) / n);
+}
+
+// Partial words: one 64-bit store carries the value and the epoch together.
+__device__ __forceinline__ void st_word(unsigned long long *p, float v, unsigned epoch)
+{
+    const unsigned long long w = ((unsigned long long)epoch << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ ulonglong2 ld_words2(const unsigned long long *p)
+{
+    ulonglong2 v;
+    asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(v.x), "=l"(v.y) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ unsigned long long ld_word(const unsigned long long *p)
+{
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ float word_val(unsigned long long w) { return __uint_as_float((unsigned)w); }
+__device__ __forceinline__ bool word_ok(unsigned long long w, unsigned epoch) { return (unsigned)(w >> 32) == epoch; }
+
+// Segment, row offset, k block and part of box b of a phase.
+struct BoxAt {
+    int si, row0, kb, sub, rt;
+};
+__device__ __forceinline__ BoxAt box_at(const StPhase &P, int b)
+{
+    BoxAt o;
+    o.rt = b / P.bpr;
+    const int w = b - o.rt * P.bpr;
+    if (P.kind == kGU) {
+        o.sub = w / P.KB;
+        o.kb = w - o.sub * P.KB;
+        o.si = o.sub;
+        o.row0 = o.rt * kStBox;
+    } else {
+        o.sub = 0;
+        o.kb = w;
+        int si = 0;
+        while (si + 1 < P.nseg && o.rt >= P.seg[si + 1].rt0) ++si;
+        o.si = si;
+        o.row0 = (o.rt - P.seg[si].rt0) * kStBox;
+    }
+    return o;
+}
+
+// Sums of partial words: elements i0..i0+3 of token t, part `sub` of a row
+// tile of phase Q (its n partials start at slot0), polled until every word carries the epoch (bounded).  Sums
+// run in slot order.  On giving up the status word is set and *ok cleared.
+__device__ __forceinline__ float4 sum4(const StPhase &Q, int n, int slot0, int sub, int t, int i0, int T,
+                                       unsigned epoch, bool *ok_out, unsigned *status)
+{
+    const size_t stride = (size_t)Q.nsub * T * kStBox;
+    const unsigned long long *p = Q.part + ((size_t)slot0 * Q.nsub + sub) * T * kStBox + t * kStBox + i0;
+    uint64_t t0 = 0;
+    for (;;) {
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        bool ok = true;
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const ulonglong2 a = ld_words2(p + j * stride);
+            const ulonglong2 b = ld_words2(p + j * stride + 2);
+            ok = ok && word_ok(a.x, epoch) && word_ok(a.y, epoch) && word_ok(b.x, epoch) && word_ok(b.y, epoch);
+            s[0] += word_val(a.x);
+            s[1] += word_val(a.y);
+            s[2] += word_val(b.x);
+            s[3] += word_val(b.y);
+        }
+        if (ok) return make_float4(s[0], s[1], s[2], s[3]);
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | kWaitExchange);
+            *ok_out = false;
+            return make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+// One element (part 0) of a row tile of phase Q, polled like sum4.
+__device__ __forceinline__ float sum1(const StPhase &Q, int n, int slot0, int t, int i, int T, unsigned epoch,
+                                      bool *ok_out, unsigned *status)
+{
+    const size_t stride = (size_t)Q.nsub * T * kStBox;
+    const unsigned long long *p = Q.part + (size_t)slot0 * Q.nsub * T * kStBox + t * kStBox + i;
+    uint64_t t0 = 0;
+    for (;;) {
+        float s = 0.f;
+        bool ok = true;
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) {
+            const unsigned long long w = ld_word(p + j * stride);
+            ok = ok && word_ok(w, epoch);
+            s += word_val(w);
+        }
+        if (ok) return s;
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | kWaitExchange);
+            *ok_out = false;
+            return 0.f;
+        }
+    }
+}
+
+// This warp's sums for one piece into its partial block (zeros: the warp had
+// no box of the piece).  Column c of the MMA result is token c (D: c >= T are
+// the lo columns); the z sums are reduced over the warp's row groups.
+__device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&cacc)[4][4],
+                                            const float (&zacc)[kStMaxT], bool zeros, int Tp, int T, int r,
+                                            int rr, int lane)
+{
+    const int g = lane >> 2, t4 = lane & 3;
+    const int col = 2 * t4;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+        const int row = m * 16 + g;
+        if (col < Tp) {
+            wb[col * kStBox + row] = zeros ? 0.f : cacc[m][0];
+            wb[col * kStBox + row + 8] = zeros ? 0.f : cacc[m][2];
+        }
+        if (col + 1 < Tp) {
+            wb[(col + 1) * kStBox + row] = zeros ? 0.f : cacc[m][1];
+            wb[(col + 1) * kStBox + row + 8] = zeros ? 0.f : cacc[m][3];
+        }
+    }
+    if (r > 0) {
+        const int zk = lane & (rr - 1), zg = lane / rr;
+#pragma unroll
+        for (int t = 0; t < kStMaxT; ++t) {
+            if (t < T) {
+                float v = zacc[t];
+                for (int o = rr; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+                if (zg == 0 && zk < r) wb[zoff + t * r + zk] = zeros ? 0.f : v;
+            }
+        }
+    }
+}
+
+// z contribution of one box: zacc[t] += sum over the box's 64 V rows i of
+// x[t][i] * V[i][k] for this lane's rank k = lane % RR; the lanes with the same
+// rank split the rows (RR = r rounded up to a power of two).  Fully unrolled
+// so that all shared-memory loads of a box are in flight together.
+template <int RR>
+__device__ __forceinline__ void z_box(const bf16 *__restrict__ vb, const bf16 *__restrict__ xr, int xsb, int r,
+                                      int T, bool lo, int lane, float (&zacc)[kStMaxT])
+{
+    constexpr int NG = 32 / RR, NI = kStBox / NG;
+    const int zk = lane % RR, zg = lane / RR;
+    if (zk >= r) return;
+    float vv[NI];
+#pragma unroll
+    for (int m = 0; m < NI; ++m) vv[m] = __bfloat162float(vb[(zg + NG * m) * r + zk]);
+#pragma unroll
+    for (int t = 0; t < kStMaxT; ++t) {
+        if (t < T) {
+            float acc = zacc[t];
+#pragma unroll
+            for (int m = 0; m < NI; ++m) {
+                const int i = zg + NG * m;
+                float xv = __bfloat162float(xr[t * xsb + i]);
+                if (lo) xv += __bfloat162float(xr[(T + t) * xsb + i]);
+                acc = fmaf(xv, vv[m], acc);
+            }
+            zacc[t] = acc;
+        }
+    }
+}
+
+// Ring wait: a non-blocking test first (the stage is usually loaded long
+// before its consumer reaches it), then the bounded wait.
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, unsigned parity, unsigned *status)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    return mbar_wait(bar, parity, status, kWaitRingFull);
+}
+
+__device__ __forceinline__ bool ring_wait_empty(uint64_t *bar, unsigned parity, unsigned *status)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    return mbar_wait(bar, parity, status, kWaitRingEmpty);
+}
+
+// Copies addressed by shared-memory offsets (no address conversion per box).
+__device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsigned bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+// ------------------------------------------------------------------ kernel
+struct Piece {
+    int rt, sub, si, row0, j0, nb, kb0;  // boxes j0 .. j0+nb-1 of the CTA's phase range, k blocks kb0..
+    int slot;                            // this CTA's partial slot of the row tile
+};
+
+__global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_constant__ StArgs a)
+{
+    extern __shared__ __align__(1024) char smem_raw[];
+    char *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x, G = gridDim.x;
+    const int T = a.T, r = a.r;
+    const int vblk = kStBox * r * 2, vblk16 = (vblk + 15) & ~15;
+
+    // shared memory carve
+    char *ring_w = smem;
+    char *ring_v = ring_w + (size_t)a.nst * kStBoxBytes;
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring_v + (size_t)a.nst * vblk16);
+    uint64_t *empty = full + a.nst;
+    char *aux_us = reinterpret_cast<char *>(empty + a.nst);
+    uint32_t *xst = reinterpret_cast<uint32_t *>(aux_us + (size_t)a.maxp * a.us_bytes);
+    float *wbuf = reinterpret_cast<float *>(xst + (size_t)(2 * T) * a.xs32);  // [maxp][8][wb_floats]
+    float *zsum = wbuf + (size_t)a.maxp * kWarps * a.wb_floats;                     // [maxp][T][r]
+    Piece *pcs = reinterpret_cast<Piece *>(zsum + a.maxp * kStMaxT * kStMaxR);
+    // [0] consumers gave up (written only by consumers; read for control
+    // right after a consumer barrier), [1] pieces, [2] producer gave up
+    int *gnp = reinterpret_cast<int *>(pcs + a.maxp);  // [maxnk] partials of each staged input block
+    int *gs0 = gnp + a.maxnk;                           // [maxnk] their first slot
+    volatile int *flags = reinterpret_cast<volatile int *>(gs0 + a.maxnk);
+
+    if (tid == 0) {
+        for (int i = 0; i < a.nst; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        flags[0] = flags[1] = flags[2] = 0;
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ------------------------------------------------------- producer
+        // Per box only register arithmetic and the copies: the phase's fields
+        // are read once per phase, box coordinates advance incrementally.
+        if (lane != 0) return;
+        const unsigned sbytes = (unsigned)(kStBoxBytes + vblk);
+        const uint32_t w_base = smem_u32(ring_w), v_base = smem_u32(ring_v);
+        int s = 0;
+        unsigned ph = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int phi = 0; phi < a.nph && ok; ++phi) {
+            const int nbox = a.ph[phi].nbox, ncta = a.ph[phi].ncta;
+            const int b0 = st_lo(nbox, c, ncta), b1 = st_lo(nbox, c + 1, ncta);
+            if (b0 >= b1) continue;
+            const bool gu = a.ph[phi].kind == kGU;
+            const int KB = a.ph[phi].KB, bpr = a.ph[phi].bpr, nseg = a.ph[phi].nseg;
+            const CUtensorMap *map[3];
+            const bf16 *Vp[3];
+            int rt0[3];
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+                map[j] = a.ph[phi].seg[j].map;
+                Vp[j] = a.ph[phi].seg[j].V;
+                rt0[j] = j < nseg ? a.ph[phi].seg[j].rt0 : 0x7fffffff;
+            }
+            int rt = b0 / bpr, w = b0 - rt * bpr;
+            for (int b = b0; b < b1; ++b) {
+                // segment, row offset and k block of box (rt, w)
+                int si, kb, row0;
+                if (gu) {
+                    si = w >= KB ? 1 : 0;
+                    kb = w - si * KB;
+                    row0 = rt * kStBox;
+                } else {
+                    si = rt >= rt0[2] ? 2 : (rt >= rt0[1] ? 1 : 0);
+                    kb = w;
+                    row0 = (rt - (si == 2 ? rt0[2] : si == 1 ? rt0[1] : 0)) * kStBox;
+                }
+                const CUtensorMap *m = si == 2 ? map[2] : si == 1 ? map[1] : map[0];
+                const bf16 *V = si == 2 ? Vp[2] : si == 1 ? Vp[1] : Vp[0];
+                if (flags[0] || !ring_wait_empty(&empty[s], ph ^ 1u, a.status)) {
+                    ok = false;
+                    break;
+                }
+                uint64_t *fb = &full[s];
+                mbar_expect_tx(fb, sbytes);
+                tma_load_2d_u32(w_base + (uint32_t)s * kStBoxBytes, m, kb * kStBox, row0, fb);
+                if (vblk) bulk_g2s_u32(v_base + (uint32_t)s * vblk16, V + (size_t)kb * kStBox * r, (unsigned)vblk, fb);
+                ++issued;
+                if (++s == a.nst) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+                if (++w == bpr) {
+                    w = 0;
+                    ++rt;
+                }
+            }
+        }
+        if (!ok) {
+            // let the copies in flight land before the CTA exits
+            flags[2] = 1;
+            const int n = issued < a.nst ? issued : a.nst;
+            for (int i = 0; i < n; ++i) {
+                s = (s == 0 ? a.nst : s) - 1;
+                if (s == a.nst - 1) ph ^= 1u;
+                mbar_wait(&full[s], ph, a.status, kWaitRingFull);
+            }
+        }
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers
+    const int g = lane >> 2, t4 = lane & 3;
+    const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row within a 16-row group
+    const int lchunk = lane >> 4;
+    const int rr = a.rr > 0 ? a.rr : 1;
+    int qbase = 0;  // CTA-local sequence number of the phase's first box
+
+    for (int phi = 0; phi < a.nph && !flags[0]; ++phi) {
+        const StPhase &P = a.ph[phi];
+        const int b0 = st_lo(P.nbox, c, P.ncta), b1 = st_lo(P.nbox, c + 1, P.ncta);
+        const int nbx = b1 - b0;
+        const int kind = P.kind, KB = P.KB, Tp = kind == kD ? 2 * T : T;
+        if (nbx > 0) {
+            // input blocks kbs .. kbs + nk - 1 (mod KB), staged at positions 0..nk-1
+            const int kbs = box_at(P, b0).kb;
+            const int nk = min(nbx, KB);
+            if (P.prev >= 0) {
+                const StPhase &Q = a.ph[P.prev];
+                for (int j = tid; j < nk; j += kThreads) {
+                    int kb = kbs + j;
+                    if (kb >= KB) kb -= KB;
+                    gnp[j] = Q.np[kb];
+                    gs0[j] = Q.slot0[kb];
+                }
+            }
+            // pieces: runs of boxes with the same (row tile, part)
+            if (tid == 0) {
+                int n = 0, b = b0;
+                while (b < b1 && n < a.maxp) {
+                    const BoxAt bx = box_at(P, b);
+                    int end = (bx.rt + 1) * P.bpr;
+                    if (kind == kGU && bx.sub == 0) end = bx.rt * P.bpr + KB;
+                    if (end > b1) end = b1;
+                    Piece pc;
+                    pc.rt = bx.rt;
+                    pc.sub = bx.sub;
+                    pc.si = bx.si;
+                    pc.row0 = bx.row0;
+                    pc.j0 = b - b0;
+                    pc.nb = end - b;
+                    pc.kb0 = bx.kb;
+                    pc.slot = P.slot0[bx.rt] + (c - st_owner(bx.rt * P.bpr, P.nbox, P.ncta));
+                    pcs[n++] = pc;
+                    b = end;
+                }
+                flags[1] = n;
+            }
+            consumer_sync();
+            const int npc = flags[1];
+
+            // prefetch U rows and s of every piece (independent of the input)
+            for (int i = 0; i < npc; ++i) {
+                const Piece pc = pcs[i];
+                const StSeg &sg = P.seg[pc.si];
+                const int rows = min(kStBox, sg.out - pc.row0);
+                char *dst = aux_us + (size_t)i * a.us_bytes;
+                if (r > 0) prefetch(dst, sg.U + (size_t)pc.row0 * r, rows * r * 2);
+                prefetch(dst + ((kStBox * r * 2 + 16 + 15) & ~15), sg.s + pc.row0, rows * 4);
+            }
+
+            bf16 *xs = reinterpret_cast<bf16 *>(xst);
+            const int xsb = 2 * a.xs32;  // x stage row stride (bf16)
+            if (P.prev >= 0) {
+                const StPhase &Q = a.ph[P.prev];
+                // groups of 4 elements of one token of one input block
+                for (int it = tid; it < nk * T * 16; it += kThreads) {
+                    const int pos = it / (T * 16);
+                    const int rem = it - pos * T * 16;
+                    const int t = rem >> 4, i0 = (rem & 15) * 4;
+                    int kb = kbs + pos;
+                    if (kb >= KB) kb -= KB;
+                    const int col = pos * kStBox + i0;
+                    bool ok = true;
+                    const int qn = gnp[pos], qs = gs0[pos];
+                    if (kind == kD) {
+                        const float4 g4 = sum4(Q, qn, qs, 0, t, i0, T, a.epoch, &ok, a.status);
+                        const float4 u4 = ok ? sum4(Q, qn, qs, 1, t, i0, T, a.epoch, &ok, a.status)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+                        if (!ok) {
+                            flags[0] = 1;
+                            break;
+                        }
+                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float hv = gelu_tanh_f32(gv[e]) * uv[e];
+                            const bf16 hi = __float2bfloat16_rn(hv);
+                            xs[t * xsb + col + e] = hi;
+                            xs[(T + t) * xsb + col + e] = __float2bfloat16_rn(hv - __bfloat162float(hi));
+                        }
+                    } else {
+                        const float4 v4 = sum4(Q, qn, qs, 0, t, i0, T, a.epoch, &ok, a.status);
+                        if (!ok) {
+                            flags[0] = 1;
+                            break;
+                        }
+                        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
+                        const bool wr = P.wy && kb >= b0 && kb < b1;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bf16 b = __float2bfloat16_rn(v[e]);
+                            xs[t * xsb + col + e] = b;
+                            if (wr) P.wy[(size_t)t * P.K + (size_t)kb * kStBox + i0 + e] = b;
+                        }
+                    }
+                }
+            } else {
+                for (int it = tid; it < nk * T * kStBox; it += kThreads) {
+                    const int pos = it / (T * kStBox);
+                    const int rem = it - pos * T * kStBox;
+                    const int t = rem / kStBox, i = rem - t * kStBox;
+                    int kb = kbs + pos;
+                    if (kb >= KB) kb -= KB;
+                    xs[t * xsb + pos * kStBox + i] = a.x[(size_t)t * P.K + (size_t)kb * kStBox + i];
+                }
+            }
+            cp_async_wait_all();
+            consumer_sync();
+            if (flags[0]) break;  // every thread has passed its input waits
+
+            // ---- boxes: box j of the range goes to warp j % 8
+            float cacc[4][4];
+            float zacc[kStMaxT];
+#pragma unroll
+            for (int m = 0; m < 4; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
+#pragma unroll
+            for (int t = 0; t < kStMaxT; ++t) zacc[t] = 0.f;
+            int cur = -1;  // piece of the accumulators
+            int pi = 0;
+            float *wbw = wbuf + (size_t)warp * a.wb_floats;
+            const size_t wbp = (size_t)kWarps * a.wb_floats;  // stride between pieces
+            for (int j = warp; j < nbx; j += kWarps) {
+                while (pi + 1 < npc && j >= pcs[pi + 1].j0) ++pi;
+                if (pi != cur) {
+                    if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zacc, false, Tp, T, r, rr, lane);
+                    for (int p = cur + 1; p < pi; ++p)
+                        flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zacc, true, Tp, T, r, rr, lane);
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
+#pragma unroll
+                    for (int t = 0; t < kStMaxT; ++t) zacc[t] = 0.f;
+                    cur = pi;
+                }
+                const int q = qbase + j;
+                const int s = q % a.nst;
+                const unsigned ph = (unsigned)((q / a.nst) & 1);
+                int w_ok = 1;
+                if (lane == 0) w_ok = !flags[0] && ring_wait(&full[s], ph, a.status);
+                w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+                if (!w_ok) {
+                    if (lane == 0) flags[0] = 1;
+                    break;
+                }
+                int pos = pcs[pi].kb0 + (j - pcs[pi].j0) - kbs;
+                if (pos < 0) pos += KB;
+                const uint32_t sb = smem_u32(ring_w + (size_t)s * kStBoxBytes);
+#pragma unroll
+                for (int kin = 0; kin < 4; ++kin) {
+                    uint32_t b0r = 0u, b1r = 0u;
+                    if (g < Tp) {
+                        const uint32_t *xr = xst + g * a.xs32 + pos * (kStBox / 2) + kin * 8 + t4;
+                        b0r = xr[0];
+                        b1r = xr[4];
+                    }
+                    const int chunk = kin * 2 + lchunk;
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) {
+                        const int row = m * 16 + lrow;
+                        uint32_t af[4];
+                        ldmatrix_x4(af, sb + row * 128 + ((chunk ^ (row & 7)) << 4));
+                        mma_16816(cacc[m], af, b0r, b1r);
+                    }
+                }
+                if (r > 0) {
+                    const bf16 *vb = reinterpret_cast<const bf16 *>(ring_v + (size_t)s * vblk16);
+                    const bf16 *xr = xs + pos * kStBox;
+                    const bool lo = kind == kD;
+                    switch (rr) {
+                    case 1: z_box<1>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    case 2: z_box<2>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    case 4: z_box<4>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    case 8: z_box<8>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    case 16: z_box<16>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    default: z_box<32>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            qbase += nbx;
+            if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zacc, false, Tp, T, r, rr, lane);
+            for (int p = cur + 1; p < npc; ++p)
+                flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zacc, true, Tp, T, r, rr, lane);
+            consumer_sync();
+            if (flags[0]) break;  // every box loop has ended: all threads agree
+
+            // ---- phase end: z per piece, then p = s * acc + U z per row
+            for (int it = tid; it < npc * T * r; it += kThreads) {
+                const int p = it / (T * r), rem = it - p * T * r;
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w)
+                    sum += wbuf[((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff + rem];
+                zsum[p * kStMaxT * kStMaxR + rem] = sum;
+            }
+            consumer_sync();
+            for (int it = tid; it < npc * T * kStBox; it += kThreads) {
+                const int p = it / (T * kStBox), rem = it - p * T * kStBox;
+                const int t = rem >> 6, row = rem & 63;
+                const Piece pc = pcs[p];
+                const StSeg &sg = P.seg[pc.si];
+                float acc = 0.f, acc_lo = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    const float *wb = wbuf + ((size_t)p * kWarps + w) * a.wb_floats;
+                    acc += wb[t * kStBox + row];
+                    if (kind == kD) acc_lo += wb[(T + t) * kStBox + row];
+                }
+                acc += acc_lo;
+                float v = 0.f;
+                if (pc.row0 + row < sg.out) {
+                    const char *us = aux_us + (size_t)p * a.us_bytes;
+                    const bf16 *Ur = reinterpret_cast<const bf16 *>(
+                        us + (reinterpret_cast<uintptr_t>(sg.U + (size_t)pc.row0 * r) & 15));
+                    const float *sr = reinterpret_cast<const float *>(
+                        us + ((kStBox * r * 2 + 16 + 15) & ~15) + (reinterpret_cast<uintptr_t>(sg.s + pc.row0) & 15));
+                    v = sr[row] * acc;
+                    const float *zp = zsum + p * kStMaxT * kStMaxR + t * r;
+                    for (int k = 0; k < r; ++k) v = fmaf(__bfloat162float(Ur[row * r + k]), zp[k], v);
+                }
+                unsigned long long *sp = P.part + (size_t)pc.slot * P.nsub * T * kStBox;
+                st_word(sp + ((size_t)pc.sub * T + t) * kStBox + row, v, a.epoch);
+                // GU: a CTA holding one part of a pair adds zeros for the other
+                if (kind == kGU) {
+                    const bool has_other = pc.sub == 0 ? (p + 1 < npc && pcs[p + 1].rt == pc.rt)
+                                                       : (p > 0 && pcs[p - 1].rt == pc.rt);
+                    if (!has_other) st_word(sp + ((size_t)(1 - pc.sub) * T + t) * kStBox + row, 0.f, a.epoch);
+                }
+            }
+        }
+
+        // ---- outputs no phase reads (k, v; the last layer's): assigned row tiles
+        if (P.xw_n > 0) {
+            const StPhase &X = a.ph[P.xw_ph];
+            for (int w = c; w < P.xw_n; w += G) {
+                const int rt = P.xw_rt0 + w;
+                int si = 0;
+                while (si + 1 < X.nseg && rt >= X.seg[si + 1].rt0) ++si;
+                const StSeg &sg = X.seg[si];
+                const int row0 = (rt - sg.rt0) * kStBox;
+                if (tid < T * kStBox) {
+                    const int t = tid >> 6, row = tid & 63;
+                    bool ok = true;
+                    const float v = sum1(X, X.np[rt], X.slot0[rt], t, row, T, a.epoch, &ok, a.status);
+                    if (!ok) flags[0] = 1;
+                    else if (row0 + row < sg.out)
+                        sg.y[(size_t)t * sg.out + row0 + row] = __float2bfloat16_rn(v);
+                }
+            }
+        }
+        consumer_sync();
+    }
+    cp_async_wait_all();
+}
+
+// ------------------------------------------------------------------- host
+struct StackPlan {
+    int device = -1;
+    int L = 0, T = 0, r = 0, hidden = 0;
+    int G = 0, smem = 0;
+    unsigned epoch = 0;
+    std::vector<StArgs> chunks;           // one launch per chunk of at most 24 layers
+    std::vector<const bf16 *> chunk_x;    // input of each chunk (null: the caller's x)
+    void *dmem = nullptr;  // tensor maps, partial tables, partial words
+};
+
+static int cdiv_i(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
+
+}  // namespace wl
+
+using namespace wl;
+
+struct wl_stack_s {
+    StackPlan p;
+    std::mutex mu;
+};
+
+static wl_status check_layer_proj(const wl_proj &p, int64_t out, int64_t r, const char *what, int64_t l)
+{
+    if (!p.W0 || !p.s || (r > 0 && (!p.U || !p.V)))
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_create: layer %lld %s: NULL pointer", (long long)l, what);
+    if (p.out != out)
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_create: layer %lld %s: out = %lld, expected %lld", (long long)l,
+                    what, (long long)p.out, (long long)out);
+    if ((reinterpret_cast<uintptr_t>(p.W0) & 15) || (r > 0 && (reinterpret_cast<uintptr_t>(p.V) & 15)))
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_create: layer %lld %s: W0 and V must be 16-byte aligned",
+                    (long long)l, what);
+    return WL_OK;
+}
+
+extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, const wl_layer_out *outs,
+                                     int64_t L, int64_t T, int64_t hidden, int64_t r)
+{
+    if (!out) return fail(WL_ERR_INVALID_ARG, "wl_stack_create: out is NULL");
+    *out = nullptr;
+    if (!layers || !outs || L < 1 || L > 4096)
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_create: need 1 <= L <= 4096 layers and outputs");
+    if (T < 1 || T > kStMaxT)
+        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: T = %lld; the stack kernel takes 1..%d tokens", (long long)T,
+                    kStMaxT);
+    if (r < 0 || r > kStMaxR)
+        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: r = %lld; the stack kernel takes 0..%d", (long long)r,
+                    kStMaxR);
+    const int64_t qd = layers[0].q.out, kvd = layers[0].k.out, vd = layers[0].v.out, inter = layers[0].gate.out;
+    if (hidden < 64 || hidden % 64 || qd < 64 || qd % 64 || inter < 64 || inter % 64 || kvd < 1 || vd < 1)
+        return fail(WL_ERR_UNSUPPORTED,
+                    "wl_stack_create: hidden (%lld), q.out (%lld) and gate.out (%lld) must be multiples of 64",
+                    (long long)hidden, (long long)qd, (long long)inter);
+    for (int64_t l = 0; l < L; ++l) {
+        const wl_layer &ly = layers[l];
+        wl_status s;
+        if ((s = check_layer_proj(ly.q, qd, r, "q", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.k, kvd, r, "k", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.v, vd, r, "v", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.o, hidden, r, "o", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.gate, inter, r, "gate", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.up, inter, r, "up", l)) != WL_OK) return s;
+        if ((s = check_layer_proj(ly.down, hidden, r, "down", l)) != WL_OK) return s;
+        const wl_layer_out &o = outs[l];
+        if (!o.yq || !o.yk || !o.yv || !o.yo || !o.ym)
+            return fail(WL_ERR_INVALID_ARG, "wl_stack_create: layer %lld: NULL output buffer", (long long)l);
+    }
+    wl_status st = WL_OK;
+    const DeviceInfo *di = device_info(&st);
+    if (!di) return st;
+
+    StackPlan pl;
+    pl.device = di->device;
+    pl.L = (int)L;
+    pl.T = (int)T;
+    pl.r = (int)r;
+    pl.hidden = (int)hidden;
+    pl.G = di->sm_count;
+    const int G = pl.G;
+
+    // ---- phases (host copy; device pointers filled in below)
+    struct HostPhase {
+        StPhase P;
+        const wl_proj *proj[3];
+        std::vector<int> np, slot0;
+        int nslots;
+    };
+    std::vector<HostPhase> hp(4 * L);
+    for (int64_t l = 0; l < L; ++l) {
+        const wl_layer &ly = layers[l];
+        const wl_layer_out &o = outs[l];
+        for (int k = 0; k < 4; ++k) {
+            HostPhase &h = hp[4 * l + k];
+            StPhase &P = h.P;
+            memset(&P, 0, sizeof(P));
+            P.kind = k;
+            int64_t K = 0;
+            if (k == kQKV) {
+                K = hidden;
+                P.nseg = 3;
+                h.proj[0] = &ly.q;
+                h.proj[1] = &ly.k;
+                h.proj[2] = &ly.v;
+                P.seg[0].y = static_cast<bf16 *>(o.yq);
+                P.seg[1].y = static_cast<bf16 *>(o.yk);
+                P.seg[2].y = static_cast<bf16 *>(o.yv);
+            } else if (k == kO) {
+                K = qd;
+                P.nseg = 1;
+                h.proj[0] = &ly.o;
+                P.seg[0].y = static_cast<bf16 *>(o.yo);
+            } else if (k == kGU) {
+                K = hidden;
+                P.nseg = 2;
+                h.proj[0] = &ly.gate;
+                h.proj[1] = &ly.up;
+            } else {
+                K = inter;
+                P.nseg = 1;
+                h.proj[0] = &ly.down;
+                P.seg[0].y = static_cast<bf16 *>(o.ym);
+            }
+            P.K = (int)K;
+            P.KB = (int)(K / 64);
+            int rt = 0;
+            for (int j = 0; j < P.nseg; ++j) {
+                P.seg[j].out = (int)h.proj[j]->out;
+                P.seg[j].s = h.proj[j]->s;
+                P.seg[j].U = static_cast<const bf16 *>(h.proj[j]->U);
+                P.seg[j].V = static_cast<const bf16 *>(h.proj[j]->V);
+                P.seg[j].nrt = cdiv_i(h.proj[j]->out, 64);
+                P.seg[j].rt0 = (k == kGU) ? 0 : rt;
+                if (k != kGU) rt += P.seg[j].nrt;
+            }
+            if (k == kGU) {
+                P.nrt = P.seg[0].nrt;
+                P.bpr = 2 * P.KB;
+                P.nsub = 2;
+            } else {
+                P.nrt = rt;
+                P.bpr = P.KB;
+                P.nsub = 1;
+            }
+            P.nbox = P.nrt * P.bpr;
+            // O is small: half the CTAs keep its row tiles' partial counts low
+            const int want = (k == kO) ? (G + 1) / 2 : G;
+            P.ncta = P.nbox < want ? P.nbox : want;
+            // input: layer 0's QKV reads x; otherwise the previous phase
+            // (row tile kb of the producer holds input block kb: q is QKV's
+            // first segment and q.out is a multiple of 64)
+            P.prev = (l == 0 && k == kQKV) ? -1 : (int)(4 * l + k - 1);
+            if (k == kO) P.wy = static_cast<bf16 *>(o.yq);
+            if (k == kGU) P.wy = static_cast<bf16 *>(o.yo);
+            if (k == kQKV && l > 0) P.wy = static_cast<bf16 *>(outs[l - 1].ym);
+            // outputs nobody reads: k and v (stored during O), the last ym
+            if (k == kO) {
+                P.xw_ph = (int)(4 * l + kQKV);
+                P.xw_rt0 = cdiv_i(qd, 64);
+                P.xw_n = cdiv_i(kvd, 64) + cdiv_i(vd, 64);
+            }
+            if (k == kD && l == L - 1) {
+                P.xw_ph = (int)(4 * l + kD);
+                P.xw_rt0 = 0;
+                P.xw_n = cdiv_i(hidden, 64);
+            }
+            // partials per row tile: the CTAs whose ranges touch it
+            h.np.resize(P.nrt);
+            h.slot0.resize(P.nrt);
+            int ns = 0;
+            for (int t = 0; t < P.nrt; ++t) {
+                const int bfirst = t * P.bpr, blast = bfirst + P.bpr - 1;
+                const int c0 = (int)((((int64_t)bfirst + 1) * P.ncta - 1) / P.nbox);
+                const int c1 = (int)((((int64_t)blast + 1) * P.ncta - 1) / P.nbox);
+                h.np[t] = c1 - c0 + 1;
+                h.slot0[t] = ns;
+                ns += h.np[t];
+            }
+            h.nslots = ns;
+        }
+    }
+
+    // ---- work bounds per CTA: pieces, staged input blocks
+    int maxp = 1, nkmax = 1;
+    for (auto &h : hp) {
+        const StPhase &P = h.P;
+        for (int cc = 0; cc < P.ncta; ++cc) {
+            const int b0 = (int)((int64_t)P.nbox * cc / P.ncta), b1 = (int)((int64_t)P.nbox * (cc + 1) / P.ncta);
+            if (b0 >= b1) continue;
+            int n = 0;
+            for (int b = b0; b < b1;) {
+                const int rt = b / P.bpr, w = b - rt * P.bpr;
+                int end = (rt + 1) * P.bpr;
+                if (P.kind == kGU && w < P.KB) end = rt * P.bpr + P.KB;
+                if (end > b1) end = b1;
+                ++n;
+                b = end;
+            }
+            if (n > maxp) maxp = n;
+            const int nk = std::min(b1 - b0, P.KB);
+            if (nk > nkmax) nkmax = nk;
+        }
+    }
+
+    // ---- shared memory
+    int rr = 1;
+    while (rr < r) rr <<= 1;
+    const int vblk16 = ((int)(64 * r * 2) + 15) & ~15;
+    const int us_bytes = ((int)(64 * r * 2) + 16 + 15) / 16 * 16 + (64 * 4 + 16 + 15) / 16 * 16;
+    int xs32 = (nkmax * 64 + 8) / 2;  // row stride (u32); 4 mod 32 keeps the B-operand reads conflict-free
+    xs32 = (xs32 + 31) / 32 * 32 + 4;
+    const int wb_floats = 2 * (int)T * 64 + (int)T * (int)(r > 0 ? r : 1);
+    const int fixed = 1024 + maxp * us_bytes + 2 * (int)T * xs32 * 4 + maxp * kWarps * wb_floats * 4 +
+                      maxp * kStMaxT * kStMaxR * 4 + maxp * (int)sizeof(Piece) + 2 * nkmax * 4 + 16 + 64;
+    const int per_stage = kStBoxBytes + vblk16 + 16;
+    int nst = (di->max_smem_optin - fixed) / per_stage;
+    if (nst > 32) nst = 32;
+    if (nst < 8)
+        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: these shapes leave room for %d ring stages", nst);
+    pl.smem = fixed + nst * per_stage;
+
+    // ---- device memory: maps, phases, np/slot0, partial words
+    size_t off = 0;
+    auto take = [&](size_t bytes, size_t align) {
+        off = (off + align - 1) / align * align;
+        const size_t o = off;
+        off += bytes;
+        return o;
+    };
+    const size_t o_maps = take(sizeof(CUtensorMap) * 7 * L, 128);
+    std::vector<size_t> o_np(4 * L), o_s0(4 * L), o_part(4 * L);
+    for (size_t i = 0; i < hp.size(); ++i) {
+        o_np[i] = take(sizeof(int) * hp[i].P.nrt, 16);
+        o_s0[i] = take(sizeof(int) * hp[i].P.nrt, 16);
+    }
+    const size_t o_tables_end = take(0, 256);
+    for (size_t i = 0; i < hp.size(); ++i)
+        o_part[i] = take(sizeof(unsigned long long) * (size_t)hp[i].nslots * hp[i].P.nsub * T * 64, 256);
+    const size_t total = off;
+
+    void *dmem = nullptr;
+    cudaError_t e = cudaMalloc(&dmem, total);
+    if (e != cudaSuccess) return cuda_fail(e, "wl_stack_create: cudaMalloc of the stack's tables and scratch");
+    char *base = static_cast<char *>(dmem);
+    std::vector<char> host(o_tables_end, 0);
+    CUtensorMap *hmaps = reinterpret_cast<CUtensorMap *>(host.data() + o_maps);
+    for (int64_t l = 0; l < L; ++l) {
+        const wl_proj *pj[7] = {&layers[l].q, &layers[l].k, &layers[l].v, &layers[l].o,
+                                &layers[l].gate, &layers[l].up, &layers[l].down};
+        const int64_t ins[7] = {hidden, hidden, hidden, qd, hidden, hidden, inter};
+        for (int j = 0; j < 7; ++j) {
+            st = tmap_2d_bf16(pj[j]->W0, ins[j], pj[j]->out, ins[j], 64, 64, &hmaps[7 * l + j]);
+            if (st != WL_OK) {
+                cudaFree(dmem);
+                return st;
+            }
+        }
+    }
+    for (size_t i = 0; i < hp.size(); ++i) {
+        HostPhase &h = hp[i];
+        const int64_t l = (int64_t)i / 4;
+        const int k = (int)(i % 4);
+        const int mj[4][3] = {{0, 1, 2}, {3, -1, -1}, {4, 5, -1}, {6, -1, -1}};
+        for (int j = 0; j < h.P.nseg; ++j)
+            h.P.seg[j].map = reinterpret_cast<const CUtensorMap *>(base + o_maps) + 7 * l + mj[k][j];
+        memcpy(host.data() + o_np[i], h.np.data(), sizeof(int) * h.P.nrt);
+        memcpy(host.data() + o_s0[i], h.slot0.data(), sizeof(int) * h.P.nrt);
+        h.P.np = reinterpret_cast<const int *>(base + o_np[i]);
+        h.P.slot0 = reinterpret_cast<const int *>(base + o_s0[i]);
+        h.P.part = reinterpret_cast<unsigned long long *>(base + o_part[i]);
+    }
+    e = cudaMemcpy(dmem, host.data(), o_tables_end, cudaMemcpyHostToDevice);
+    // partial words start at epoch 0; launches use epochs 1, 2, ...
+    if (e == cudaSuccess) e = cudaMemset(base + o_tables_end, 0, total - o_tables_end);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        cudaFree(dmem);
+        return cuda_fail(e, "wl_stack_create: table upload");
+    }
+    e = cudaFuncSetAttribute((const void *)stack_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             di->max_smem_optin);
+    if (e != cudaSuccess) {
+        cudaFree(dmem);
+        return cuda_fail(e, "cudaFuncSetAttribute(stack_kernel)");
+    }
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, stack_kernel, kStThreads, (size_t)pl.smem);
+    if (e != cudaSuccess || per_sm < 1) {
+        cudaFree(dmem);
+        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: the stack kernel does not fit on an SM (%d bytes)",
+                    pl.smem);
+    }
+
+    // launches: chunks of at most kStMaxPh / 4 layers, of about equal size
+    const int lmax = kStMaxPh / 4;
+    const int nchunk = cdiv_i(L, lmax);
+    StArgs a;
+    memset(&a, 0, sizeof(a));
+    a.T = (int)T;
+    a.r = (int)r;
+    a.rr = rr;
+    a.nst = nst;
+    a.maxp = maxp;
+    a.xs32 = xs32;
+    a.us_bytes = us_bytes;
+    a.wb_floats = wb_floats;
+    a.wb_zoff = 2 * (int)T * 64;
+    a.maxnk = nkmax;
+    a.status = di->status;
+    for (int ch = 0; ch < nchunk; ++ch) {
+        const int l0 = (int)(L * ch / nchunk), l1 = (int)(L * (ch + 1) / nchunk);
+        const int base_ph = 4 * l0;
+        a.nph = 4 * (l1 - l0);
+        for (int i = 0; i < a.nph; ++i) {
+            StPhase P = hp[base_ph + i].P;
+            if (i == 0) {
+                // the chunk's input: x, or the previous chunk's output (stored
+                // by that launch's last phase)
+                P.prev = -1;
+                P.wy = nullptr;
+            } else {
+                P.prev -= base_ph;
+            }
+            if (P.xw_n > 0) P.xw_ph -= base_ph;
+            if (i == a.nph - 1 && P.xw_n == 0) {  // chunk end: store the last layer's output
+                P.xw_ph = i;
+                P.xw_rt0 = 0;
+                P.xw_n = cdiv_i(hidden, 64);
+            }
+            a.ph[i] = P;
+        }
+        pl.chunks.push_back(a);
+        pl.chunk_x.push_back(l0 == 0 ? nullptr : static_cast<const bf16 *>(outs[l0 - 1].ym));
+    }
+    pl.dmem = dmem;
+
+    wl_stack_s *h = new (std::nothrow) wl_stack_s;
+    if (!h) {
+        cudaFree(dmem);
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_create: out of host memory");
+    }
+    h->p = pl;
+    *out = h;
+    return WL_OK;
+}
+
+extern "C" wl_status wl_stack_decode(wl_stack stk, const void *x, void *stream)
+{
+    if (!stk || !x) return fail(WL_ERR_INVALID_ARG, "wl_stack_decode: NULL stack or x");
+    if (reinterpret_cast<uintptr_t>(x) & 15) return fail(WL_ERR_INVALID_ARG, "wl_stack_decode: x must be 16-byte aligned");
+    StackPlan &pl = stk->p;
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != pl.device)
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_decode: the stack was built on device %d, current is %d", pl.device,
+                    dev);
+    unsigned epoch;
+    {
+        std::lock_guard<std::mutex> lk(stk->mu);
+        // epochs 1 .. 2^32-1; 0 marks words never written
+        if (++pl.epoch == 0) pl.epoch = 1;
+        epoch = pl.epoch;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)pl.G);
+    cfg.blockDim = dim3(kStThreads);
+    cfg.dynamicSmemBytes = (size_t)pl.smem;
+    cfg.stream = static_cast<cudaStream_t>(stream);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    for (size_t ch = 0; ch < pl.chunks.size(); ++ch) {
+        StArgs a = pl.chunks[ch];  // a copy: calls on other threads may launch at the same time
+        a.epoch = epoch;
+        a.x = pl.chunk_x[ch] ? pl.chunk_x[ch] : static_cast<const bf16 *>(x);
+        void *args[] = {&a};
+        cudaError_t e = cudaLaunchKernelExC(&cfg, (const void *)stack_kernel, args);
+        if (e != cudaSuccess) return cuda_fail(e, "wl_stack_decode: launch");
+    }
+    return WL_OK;
+}
+
+extern "C" void wl_stack_destroy(wl_stack stk)
+{
+    if (!stk) return;
+    if (stk->p.dmem) cudaFree(stk->p.dmem);
+    delete stk;
+}

@@ -24,7 +24,7 @@ def _run(wl, x, th, ydt, dev):
 
 @pytest.mark.parametrize("T", [65, 128, 200])
 @pytest.mark.parametrize("n_in,out", [(64, 16), (520, 300), (1152, 256), (136, 513)])
-@pytest.mark.parametrize("r", [0, 4, 16, 33, 128])
+@pytest.mark.parametrize("r", [0, 4, 8, 16, 33, 64, 128])
 def test_prefill_ragged(wl, orc, gpu, T, n_in, out, r):
     ydt = torch.float32 if (T + r) % 2 else torch.bfloat16
     x, th = wl_synth.linear_case(3000 + T + r, T, n_in, out, r)
@@ -83,7 +83,7 @@ def _mlp_case(seed, T, hidden, inter, r):
 
 
 @pytest.mark.parametrize("T", [9, 65, 200])
-@pytest.mark.parametrize("hidden,inter,r", [(64, 136, 3), (264, 520, 0), (128, 1000, 33)])
+@pytest.mark.parametrize("hidden,inter,r", [(64, 136, 3), (264, 520, 0), (128, 1000, 33), (128, 1000, 16), (64, 136, 8)])
 def test_prefill_mlp_small(wl, orc, gpu, T, hidden, inter, r):
     x, ths = _mlp_case(T * 7 + r, T, hidden, inter, r)
     ref = orc.mlp_geglu(x, *ths)
