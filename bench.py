@@ -233,7 +233,8 @@ def run_wl(args):
     T = 1
     nl = args.layers
     layers = build_layers(nl, nl, T, SHAPES, r, seed=rank, device=dev)
-    stack = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev)
+    stack = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev,
+                         engine=args.engine)
     gx = torch.Generator(device=dev)
     gx.manual_seed(100 + rank)
     stack.x.copy_(torch.randn(T, SHAPES["hidden"], generator=gx, device=dev).to(torch.bfloat16))
@@ -267,19 +268,36 @@ def run_wl(args):
     value = step_bytes * world / (ms * 1e-3) / 1e9
     status = wl.wl_device_status(stack.stream)
 
-    # ---- dominant kernel: the fused MLP, per-launch events on its stream ----
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(nl)]
-    mlp_ms = []
-    for _ in range(max(3, min(args.steps, 10))):
-        stack.step(mlp_events=evs)
-        stack.stream.synchronize()
-        mlp_ms.extend(a.elapsed_time(b) for a, b in evs)
-    mlp_ms_avg = statistics.mean(mlp_ms)
+    # ---- dominant kernel, timed per launch with events on its stream ----
     hbm_peak, _, peak_kind = load_peaks()
-    mb = mlp_bytes(SHAPES, T, r)
-    achieved = mb / (mlp_ms_avg * 1e-3) / 1e9
-    traffic = load_traffic()
+    if stack.engine == "stack":
+        # the step is nchunk back-to-back launches of the stack kernel, each
+        # over an equal share of the layers
+        nchunk = stack.launches_per_step
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(3, min(args.steps, 20)))]
+        for a0, a1 in evs:
+            a0.record(stack.stream)
+            stack.step()
+            a1.record(stack.stream)
+        stack.stream.synchronize()
+        launch_ms = statistics.mean(a.elapsed_time(b) for a, b in evs) / nchunk
+        kb = step_bytes / nchunk
+        kname = f"stack_kernel ({nl // nchunk} layers per launch, {nchunk} launches per step)"
+        traffic = load_traffic("stack_kernel")
+    else:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(nl)]
+        mlp_ms = []
+        for _ in range(max(3, min(args.steps, 10))):
+            stack.step(mlp_events=evs)
+            stack.stream.synchronize()
+            mlp_ms.extend(a.elapsed_time(b) for a, b in evs)
+        launch_ms = statistics.mean(mlp_ms)
+        kb = mlp_bytes(SHAPES, T, r)
+        kname = "dec_gateup_kernel + dec_down_kernel (fused GeGLU MLP call, T=1)"
+        traffic = load_traffic("dec_mlp")
+    achieved = kb / (launch_ms * 1e-3) / 1e9
 
     # ---- end to end through the public API with pinned host buffers ----
     xh = torch.empty(T, SHAPES["hidden"], dtype=torch.bfloat16).pin_memory()
@@ -317,11 +335,13 @@ def run_wl(args):
                        "step_bytes": step_bytes,
                        "us_per_token_per_layer": round(ms * 1e3 / (T * nl), 3),
                        "us_per_token_per_stack": round(ms * 1e3 / T, 2),
-                       "graph": "CUDA graph replay of the stack"},
-            "roofline": {"bound": "hbm", "kernel": "dec_mlp_kernel (fused GeGLU MLP, T=1)",
+                       "engine": stack.engine,
+                       "graph": ("one stack-kernel launch per 24 layers" if stack.engine == "stack"
+                                 else "CUDA graph replay of the per-projection calls")},
+            "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
-                         "bytes_per_launch": mb, "avg_launch_us": round(mlp_ms_avg * 1e3, 3),
+                         "bytes_per_launch": int(kb), "avg_launch_us": round(launch_ms * 1e3, 3),
                          "traffic": traffic},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                     "h2d_bytes_per_step": T * SHAPES["hidden"] * 2,
@@ -332,6 +352,8 @@ def run_wl(args):
         }
         if ck is not None:
             line["clocks"] = ck
+        if stack.engine == "stack" and not args.no_compare:
+            line["per_call_graph"] = measure_graph_engine(layers, T, r, dev)
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
         if not args.no_cpu_baseline:
@@ -340,6 +362,30 @@ def run_wl(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_graph_engine(layers, T, r, dev, steps=30):
+    """The same step through the per-projection calls replayed as a CUDA
+    graph (the other engine), for comparison."""
+    import torch
+    from rank_weight_reconstruction_wl_gb300.stack import DecoderStack
+
+    st = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev, engine="graph")
+    st.x.normal_()
+    st.capture()
+    for _ in range(3):
+        st.step()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(st.stream)
+    for _ in range(steps):
+        st.step()
+    e1.record(st.stream)
+    st.stream.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    b = layer_bytes(SHAPES, T, r) * len(layers)
+    return {"value": round(b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "us_per_token_per_layer": round(ms * 1e3 / (T * len(layers)), 3)}
 
 
 def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
@@ -414,14 +460,14 @@ def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
             "l2": f"{nlayers} weight sets rotated (larger than L2)"}
 
 
-def load_traffic():
+def load_traffic(kernel):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
     summary (null if none was taken for the current kernel)."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(p) as f:
             d = json.load(f)
-        return d.get("dec_mlp_kernel")
+        return d.get(kernel)
     except Exception:
         return None
 
@@ -435,6 +481,9 @@ def main():
     ap.add_argument("--rank", type=int, default=4, help="LoRA rank r of the theta bundles")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=2048 prefill measurement")
+    ap.add_argument("--no-compare", action="store_true", help="skip timing the per-projection graph engine")
+    ap.add_argument("--engine", default="auto", choices=["auto", "stack", "graph"],
+                    help="stack kernel (one launch per 24 layers) or per-projection CUDA graph")
     ap.add_argument("--layers", type=int, default=L_LAYERS,
                     help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()

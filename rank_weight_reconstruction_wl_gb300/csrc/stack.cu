@@ -114,6 +114,8 @@ struct StArgs {
     int wb_floats;  // floats per (piece, warp) partial block: [2T][64] sums, then [T][r] z
     int wb_zoff;    // offset of the z part (2T * 64)
     int maxnk;      // most input blocks one CTA stages in one phase
+    const int *rec; // per (phase, CTA) work records, rec_ints each (see Piece)
+    int rec_ints;
     unsigned *status;
 };
 static_assert(sizeof(StPhase) <= 256, "phase descriptor grew");
@@ -122,10 +124,7 @@ static_assert(sizeof(StArgs) <= 31 * 1024, "kernel parameter space");
 // ----------------------------------------------------------- small helpers
 // A phase's nbox boxes are shared by its first n CTAs: CTA c < n takes
 // [nbox*c/n, nbox*(c+1)/n) (at least one box, as n <= nbox); the others none.
-__device__ __forceinline__ int st_owner(int b, int nbox, int n)
-{
-    return (int)((((int64_t)b + 1) * n - 1) / nbox);
-}
+// The CTA holding box b is ((b + 1) * n - 1) / nbox.
 __device__ __forceinline__ int st_lo(int nbox, int c, int n)
 {
     return (int)((int64_t)nbox * (c < n ? c : n) / n);
@@ -151,31 +150,6 @@ __device__ __forceinline__ unsigned long long ld_word(const unsigned long long *
 }
 __device__ __forceinline__ float word_val(unsigned long long w) { return __uint_as_float((unsigned)w); }
 __device__ __forceinline__ bool word_ok(unsigned long long w, unsigned epoch) { return (unsigned)(w >> 32) == epoch; }
-
-// Segment, row offset, k block and part of box b of a phase.
-struct BoxAt {
-    int si, row0, kb, sub, rt;
-};
-__device__ __forceinline__ BoxAt box_at(const StPhase &P, int b)
-{
-    BoxAt o;
-    o.rt = b / P.bpr;
-    const int w = b - o.rt * P.bpr;
-    if (P.kind == kGU) {
-        o.sub = w / P.KB;
-        o.kb = w - o.sub * P.KB;
-        o.si = o.sub;
-        o.row0 = o.rt * kStBox;
-    } else {
-        o.sub = 0;
-        o.kb = w;
-        int si = 0;
-        while (si + 1 < P.nseg && o.rt >= P.seg[si + 1].rt0) ++si;
-        o.si = si;
-        o.row0 = (o.rt - P.seg[si].rt0) * kStBox;
-    }
-    return o;
-}
 
 // Sums of partial words: elements i0..i0+3 of token t, part `sub` of a row
 // tile of phase Q (its n partials start at slot0), polled until every word carries the epoch (bounded).  Sums
@@ -346,10 +320,28 @@ __device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsi
 }
 
 // ------------------------------------------------------------------ kernel
+// Start copying the record of phase ph_i of CTA c into its buffer (consumer
+// threads; completes with cp_async_wait_all).
+__device__ __forceinline__ void fetch_rec(int *recbuf, const int *rec, int rec_ints, int ph_i, int G, int c)
+{
+    const int *src = rec + ((size_t)ph_i * G + c) * rec_ints;
+    int *dst = recbuf + (ph_i & 1) * rec_ints;
+    for (int i = threadIdx.x; i < rec_ints / 4; i += kThreads) cp_async16(dst + 4 * i, src + 4 * i);
+}
+
 struct Piece {
     int rt, sub, si, row0, j0, nb, kb0;  // boxes j0 .. j0+nb-1 of the CTA's phase range, k blocks kb0..
     int slot;                            // this CTA's partial slot of the row tile
 };
+
+// A CTA's work in one phase, worked out on the host (int32 words):
+//   [0] b0  [1] boxes  [2] pieces  [3] kbs  [4] nk  [5..7] unused
+//   [8 ..]            maxp Pieces (8 words each)
+//   then              maxnk partial counts of the staged input blocks
+//   then              maxnk first slots of the staged input blocks
+// Records are fetched one phase ahead into shared memory (cp.async), so no
+// table lookup in global memory sits on the path between two phases.
+constexpr int kRecHead = 8;
 
 __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_constant__ StArgs a)
 {
@@ -369,12 +361,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     uint32_t *xst = reinterpret_cast<uint32_t *>(aux_us + (size_t)a.maxp * a.us_bytes);
     float *wbuf = reinterpret_cast<float *>(xst + (size_t)(2 * T) * a.xs32);  // [maxp][8][wb_floats]
     float *zsum = wbuf + (size_t)a.maxp * kWarps * a.wb_floats;                     // [maxp][T][r]
-    Piece *pcs = reinterpret_cast<Piece *>(zsum + a.maxp * kStMaxT * kStMaxR);
+    int *recbuf = reinterpret_cast<int *>(zsum + a.maxp * kStMaxT * kStMaxR);  // 2 x rec_ints
     // [0] consumers gave up (written only by consumers; read for control
-    // right after a consumer barrier), [1] pieces, [2] producer gave up
-    int *gnp = reinterpret_cast<int *>(pcs + a.maxp);  // [maxnk] partials of each staged input block
-    int *gs0 = gnp + a.maxnk;                           // [maxnk] their first slot
-    volatile int *flags = reinterpret_cast<volatile int *>(gs0 + a.maxnk);
+    // right after a consumer barrier), [2] producer gave up
+    volatile int *flags = reinterpret_cast<volatile int *>(recbuf + 2 * a.rec_ints);
 
     if (tid == 0) {
         for (int i = 0; i < a.nst; ++i) {
@@ -465,49 +455,23 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     const int lchunk = lane >> 4;
     const int rr = a.rr > 0 ? a.rr : 1;
     int qbase = 0;  // CTA-local sequence number of the phase's first box
+    fetch_rec(recbuf, a.rec, a.rec_ints, 0, G, c);
+    cp_async_wait_all();
+    consumer_sync();
 
     for (int phi = 0; phi < a.nph && !flags[0]; ++phi) {
         const StPhase &P = a.ph[phi];
-        const int b0 = st_lo(P.nbox, c, P.ncta), b1 = st_lo(P.nbox, c + 1, P.ncta);
-        const int nbx = b1 - b0;
+        const int *rec = recbuf + (phi & 1) * a.rec_ints;
+        const int b0 = rec[0], nbx = rec[1];
+        const int b1 = b0 + nbx;
         const int kind = P.kind, KB = P.KB, Tp = kind == kD ? 2 * T : T;
+        if (phi + 1 < a.nph) fetch_rec(recbuf, a.rec, a.rec_ints, phi + 1, G, c);  // lands by the phase's end
         if (nbx > 0) {
             // input blocks kbs .. kbs + nk - 1 (mod KB), staged at positions 0..nk-1
-            const int kbs = box_at(P, b0).kb;
-            const int nk = min(nbx, KB);
-            if (P.prev >= 0) {
-                const StPhase &Q = a.ph[P.prev];
-                for (int j = tid; j < nk; j += kThreads) {
-                    int kb = kbs + j;
-                    if (kb >= KB) kb -= KB;
-                    gnp[j] = Q.np[kb];
-                    gs0[j] = Q.slot0[kb];
-                }
-            }
-            // pieces: runs of boxes with the same (row tile, part)
-            if (tid == 0) {
-                int n = 0, b = b0;
-                while (b < b1 && n < a.maxp) {
-                    const BoxAt bx = box_at(P, b);
-                    int end = (bx.rt + 1) * P.bpr;
-                    if (kind == kGU && bx.sub == 0) end = bx.rt * P.bpr + KB;
-                    if (end > b1) end = b1;
-                    Piece pc;
-                    pc.rt = bx.rt;
-                    pc.sub = bx.sub;
-                    pc.si = bx.si;
-                    pc.row0 = bx.row0;
-                    pc.j0 = b - b0;
-                    pc.nb = end - b;
-                    pc.kb0 = bx.kb;
-                    pc.slot = P.slot0[bx.rt] + (c - st_owner(bx.rt * P.bpr, P.nbox, P.ncta));
-                    pcs[n++] = pc;
-                    b = end;
-                }
-                flags[1] = n;
-            }
-            consumer_sync();
-            const int npc = flags[1];
+            const int npc = rec[2], kbs = rec[3], nk = rec[4];
+            const Piece *pcs = reinterpret_cast<const Piece *>(rec + kRecHead);
+            const int *gnp = rec + kRecHead + 8 * a.maxp;  // partials of each staged input block
+            const int *gs0 = gnp + a.maxnk;                 // their first slot
 
             // prefetch U rows and s of every piece (independent of the input)
             for (int i = 0; i < npc; ++i) {
@@ -719,6 +683,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 }
             }
         }
+        cp_async_wait_all();  // the next phase's record
         consumer_sync();
     }
     cp_async_wait_all();
@@ -927,6 +892,55 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
         }
     }
 
+    // ---- per (phase, CTA) work records
+    const int rec_ints = (kRecHead + 8 * maxp + 2 * nkmax + 3) / 4 * 4;
+    auto owner = [](int b, int nbox, int n) { return (int)((((int64_t)b + 1) * n - 1) / nbox); };
+    auto make_rec = [&](int gi, int cc, int *rec) {
+        const StPhase &P = hp[gi].P;
+        const int b0 = (int)((int64_t)P.nbox * std::min(cc, P.ncta) / P.ncta);
+        const int b1 = (int)((int64_t)P.nbox * std::min(cc + 1, P.ncta) / P.ncta);
+        memset(rec, 0, sizeof(int) * rec_ints);
+        rec[0] = b0;
+        rec[1] = b1 - b0;
+        if (b1 <= b0) return;
+        int n = 0;
+        for (int b = b0; b < b1;) {
+            const int rt = b / P.bpr, w = b - rt * P.bpr;
+            const int sub = P.kind == kGU ? w / P.KB : 0;
+            int end = (rt + 1) * P.bpr;
+            if (P.kind == kGU && sub == 0) end = rt * P.bpr + P.KB;
+            if (end > b1) end = b1;
+            int si = sub;
+            if (P.kind != kGU)
+                while (si + 1 < P.nseg && rt >= P.seg[si + 1].rt0) ++si;
+            int *pc = rec + kRecHead + 8 * n;
+            pc[0] = rt;
+            pc[1] = sub;
+            pc[2] = si;
+            pc[3] = P.kind == kGU ? rt * 64 : (rt - P.seg[si].rt0) * 64;
+            pc[4] = b - b0;
+            pc[5] = end - b;
+            pc[6] = w - sub * P.KB;
+            pc[7] = hp[gi].slot0[rt] + (cc - owner(rt * P.bpr, P.nbox, P.ncta));
+            ++n;
+            b = end;
+        }
+        rec[2] = n;
+        const int kbs = (b0 % P.bpr) % P.KB, nk = std::min(b1 - b0, P.KB);
+        rec[3] = kbs;
+        rec[4] = nk;
+        if (gi > 0) {
+            // the producing phase is the previous one (a chunk's first phase
+            // reads x and ignores these)
+            const HostPhase &Q = hp[gi - 1];
+            for (int pos = 0; pos < nk; ++pos) {
+                const int kb = (kbs + pos) % P.KB;
+                rec[kRecHead + 8 * maxp + pos] = Q.np[kb];
+                rec[kRecHead + 8 * maxp + nkmax + pos] = Q.slot0[kb];
+            }
+        }
+    };
+
     // ---- shared memory
     int rr = 1;
     while (rr < r) rr <<= 1;
@@ -936,7 +950,7 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     xs32 = (xs32 + 31) / 32 * 32 + 4;
     const int wb_floats = 2 * (int)T * 64 + (int)T * (int)(r > 0 ? r : 1);
     const int fixed = 1024 + maxp * us_bytes + 2 * (int)T * xs32 * 4 + maxp * kWarps * wb_floats * 4 +
-                      maxp * kStMaxT * kStMaxR * 4 + maxp * (int)sizeof(Piece) + 2 * nkmax * 4 + 16 + 64;
+                      maxp * kStMaxT * kStMaxR * 4 + 2 * rec_ints * 4 + 16 + 64;
     const int per_stage = kStBoxBytes + vblk16 + 16;
     int nst = (di->max_smem_optin - fixed) / per_stage;
     if (nst > 32) nst = 32;
@@ -958,6 +972,7 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
         o_np[i] = take(sizeof(int) * hp[i].P.nrt, 16);
         o_s0[i] = take(sizeof(int) * hp[i].P.nrt, 16);
     }
+    const size_t o_rec = take(sizeof(int) * (size_t)rec_ints * 4 * L * G, 256);
     const size_t o_tables_end = take(0, 256);
     for (size_t i = 0; i < hp.size(); ++i)
         o_part[i] = take(sizeof(unsigned long long) * (size_t)hp[i].nslots * hp[i].P.nsub * T * 64, 256);
@@ -969,6 +984,9 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     char *base = static_cast<char *>(dmem);
     std::vector<char> host(o_tables_end, 0);
     CUtensorMap *hmaps = reinterpret_cast<CUtensorMap *>(host.data() + o_maps);
+    for (int gi = 0; gi < 4 * L; ++gi)
+        for (int cc = 0; cc < G; ++cc)
+            make_rec(gi, cc, reinterpret_cast<int *>(host.data() + o_rec) + ((size_t)gi * G + cc) * rec_ints);
     for (int64_t l = 0; l < L; ++l) {
         const wl_proj *pj[7] = {&layers[l].q, &layers[l].k, &layers[l].v, &layers[l].o,
                                 &layers[l].gate, &layers[l].up, &layers[l].down};
@@ -1031,11 +1049,13 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     a.wb_floats = wb_floats;
     a.wb_zoff = 2 * (int)T * 64;
     a.maxnk = nkmax;
+    a.rec_ints = rec_ints;
     a.status = di->status;
     for (int ch = 0; ch < nchunk; ++ch) {
         const int l0 = (int)(L * ch / nchunk), l1 = (int)(L * (ch + 1) / nchunk);
         const int base_ph = 4 * l0;
         a.nph = 4 * (l1 - l0);
+        a.rec = reinterpret_cast<const int *>(base + o_rec) + (size_t)base_ph * G * rec_ints;
         for (int i = 0; i < a.nph; ++i) {
             StPhase P = hp[base_ph + i].P;
             if (i == 0) {

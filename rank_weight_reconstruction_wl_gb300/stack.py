@@ -1,7 +1,12 @@
-"""A stack of weightless decoder layers, replayed as one CUDA graph.
+"""A stack of weightless decoder layers.
 
 Each layer is the projection set of one decoder layer: fused Q/K/V
 (wl_qkv_fused), O (wl_linear) and the fused GeGLU MLP (wl_mlp_geglu_fused).
+Two engines run it:
+  "stack"  one launch per step (per 24 layers) of the library's stack kernel
+           (wl_stack_create / wl_stack_decode), for T <= 4 and r <= 32;
+  "graph"  the per-projection calls, captured once and replayed as one CUDA
+           graph (any T and r).
 The method does not include attention, so the O projection takes the q output
 as its stand-in input, the MLP takes the O output, and the MLP output is the
 next layer's input (no norms, no residual).  Layer l uses W0 block
@@ -18,7 +23,7 @@ from dataclasses import dataclass
 
 import torch
 
-from . import mlp_workspace, wl_band_of_layer, wl_linear, wl_mlp_geglu_fused, wl_qkv_fused
+from . import WLError, WLStack, mlp_workspace, wl_band_of_layer, wl_linear, wl_mlp_geglu_fused, wl_qkv_fused
 
 
 @dataclass
@@ -36,7 +41,9 @@ class DecoderStack:
     """L layers sharing W0 per band; fixed T; inputs/outputs in device buffers."""
 
     def __init__(self, layers: list[LayerTheta], T: int, hidden: int, qdim: int, inter: int,
-                 r: int, ydt=torch.bfloat16, device=None, use_graph: bool = True):
+                 r: int, ydt=torch.bfloat16, device=None, use_graph: bool = True, engine: str = "auto"):
+        """engine: "stack", "graph" or "auto" (the stack kernel where it takes
+        the sizes, else the graph)."""
         self.layers = layers
         self.T, self.hidden, self.qdim, self.inter, self.r = T, hidden, qdim, inter, r
         self.dev = torch.device(device or "cuda")
@@ -58,9 +65,23 @@ class DecoderStack:
         lin = (T + 63) // 64 if T <= 64 else 1
         mlp = 2 if T <= 8 else 3
         self.launches_per_step = len(layers) * (2 * lin + mlp)
+        self.stk = None
+        if engine not in ("auto", "stack", "graph"):
+            raise ValueError(f"unknown engine {engine!r}")
+        if engine in ("auto", "stack"):
+            try:
+                self.stk = WLStack(layers, T, device=self.dev)
+            except WLError:
+                if engine == "stack":
+                    raise
+        self.engine = "stack" if self.stk is not None else "graph"
+        if self.stk is not None:
+            self.launches_per_step = (len(layers) + 23) // 24
 
     @property
     def out(self) -> torch.Tensor:
+        if self.stk is not None:
+            return self.stk.out
         return self.ym[(len(self.layers) - 1) % 2]
 
     def _issue(self, mlp_events=None):
@@ -79,7 +100,12 @@ class DecoderStack:
             x = ym
 
     def capture(self):
-        """Warm up once eagerly, then capture the whole stack in a graph."""
+        """Warm up once eagerly, then capture the whole stack in a graph
+        (the stack engine needs no graph: a step is one launch per 24 layers)."""
+        if self.stk is not None:
+            self.stk.decode(self.x, stream=self.stream)
+            self.stream.synchronize()
+            return
         with torch.cuda.stream(self.stream):
             self._issue()
         self.stream.synchronize()
@@ -92,6 +118,11 @@ class DecoderStack:
 
     def step(self, mlp_events=None):
         """One pass over all layers on self.stream (graph replay if captured)."""
+        if self.stk is not None:
+            if mlp_events is not None:
+                raise ValueError("per-MLP events need the graph engine")
+            self.stk.decode(self.x, stream=self.stream)
+            return
         if mlp_events is not None or self.graph is None:
             with torch.cuda.stream(self.stream):
                 self._issue(mlp_events)

@@ -21,7 +21,8 @@ def test_stack_graph_replay(wl, orc, gpu, L, G, r, T):
     from rank_weight_reconstruction_wl_gb300.stack import DecoderStack, build_layers
 
     layers = build_layers(L, G, T, SHAPES, r, seed=5, device=gpu)
-    st = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=gpu)
+    st = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=gpu,
+                      engine="graph")
     g = torch.Generator(device=gpu)
     g.manual_seed(1)
     st.x.copy_(torch.randn(T, SHAPES["hidden"], generator=g, device=gpu).to(torch.bfloat16))
