@@ -15,14 +15,14 @@
 // data dependencies between projections:
 //
 //   producer warp   walks the CTA's share of every phase in order and loads
-//                   each 64x64 W0 box (TMA, 128-byte swizzle) with the 64
-//                   matching rows of V into a ring of shared-memory stages,
-//                   waiting only for free stages;
+//                   each 64x64 W0 box with the matching 64 columns of V^T
+//                   (both TMA, 128-byte swizzle) into a ring of shared-memory
+//                   stages, waiting only for free stages;
 //   8 consumer warps  per phase: gather the phase input; then each warp takes
 //                   whole boxes (box j of the phase goes to warp j % 8) and
 //                   multiplies them on the tensor cores (mma.sync m16n8k16,
-//                   W0 rows as M, tokens as N), forming z = x V on the CUDA
-//                   cores; at the end of the phase the warps' sums are added
+//                   W0 rows, and the rank rows of V^T for z = x V, as M;
+//                   tokens as N); at the end of the phase the warps' sums are added
 //                   in warp order and p = s * acc + U z_range goes to a
 //                   global partial slot per (row tile, CTA).
 //
@@ -46,7 +46,11 @@
 // epoch makes values left by an earlier launch invisible.
 //
 // The down projection takes h as two bf16 columns per token (h = hi + lo), so
-// its tensor-core product keeps fp32 accuracy; z uses hi + lo in fp32.
+// its tensor-core product keeps fp32 accuracy (for z as well).
+//
+// V^T: each launch is preceded by a small kernel that writes V^T of every
+// projection, padded to 16 or 32 rank rows, into the stack's scratch, so that
+// V is read when the step runs and its 64-column blocks are TMA tiles.
 //
 // Every wait (ring stages, partial words) is bounded; a wait that gives up
 // sets the status word and the CTA winds down after its copies in flight
@@ -69,10 +73,10 @@ constexpr int kStBoxBytes = kStBox * kStBox * 2;
 enum StKind { kQKV = 0, kO = 1, kGU = 2, kD = 3 };
 
 struct StSeg {
-    const CUtensorMap *map;  // W0 [out, K], box 64 x 64 (device memory)
+    const CUtensorMap *map;    // W0 [out, K], box 64 x 64 (device memory)
+    const CUtensorMap *vtmap;  // V^T [rpad, K] (padded with zero rows), box 64 x rpad
     const float *s;
     const bf16 *U;
-    const bf16 *V;
     bf16 *y;   // output [T, out] (bf16)
     int out;
     int rt0;   // first row tile of this segment within the phase
@@ -105,14 +109,16 @@ struct StArgs {
     StPhase ph[kStMaxPh];
     int nph;
     const bf16 *x;  // [T, hidden] input of layer 0
-    int T, r, rr;   // rr: r rounded up to a power of two (<= 32)
+    int T, r;
     unsigned epoch;
     int nst;        // ring stages
     int maxp;       // most pieces of one CTA in one phase
     int xs32;       // x stage row stride (u32)
     int us_bytes;   // bytes per piece in the U/s area
-    int wb_floats;  // floats per (piece, warp) partial block: [2T][64] sums, then [T][r] z
+    int wb_floats;  // floats per (piece, warp) partial block: [2T][64] sums, then [2T][rpad] z
     int wb_zoff;    // offset of the z part (2T * 64)
+    int rpad;       // V^T rows per box (0, 16 or 32)
+    int stage_bytes;  // W0 box + V^T box
     int maxnk;      // most input blocks one CTA stages in one phase
     const int *rec; // per (phase, CTA) work records, rec_ints each (see Piece)
     int rec_ints;
@@ -211,10 +217,9 @@ __device__ __forceinline__ float sum1(const StPhase &Q, int n, int slot0, int t,
 
 // This warp's sums for one piece into its partial block (zeros: the warp had
 // no box of the piece).  Column c of the MMA result is token c (D: c >= T are
-// the lo columns); the z sums are reduced over the warp's row groups.
-__device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&cacc)[4][4],
-                                            const float (&zacc)[kStMaxT], bool zeros, int Tp, int T, int r,
-                                            int rr, int lane)
+// the lo columns); rows of zc are ranks.
+__device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&cacc)[4][4], const float (&zc)[2][4],
+                                            bool zeros, int Tp, int rpad, int lane)
 {
     const int g = lane >> 2, t4 = lane & 3;
     const int col = 2 * t4;
@@ -230,45 +235,19 @@ __device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&c
             wb[(col + 1) * kStBox + row + 8] = zeros ? 0.f : cacc[m][3];
         }
     }
-    if (r > 0) {
-        const int zk = lane & (rr - 1), zg = lane / rr;
 #pragma unroll
-        for (int t = 0; t < kStMaxT; ++t) {
-            if (t < T) {
-                float v = zacc[t];
-                for (int o = rr; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (zg == 0 && zk < r) wb[zoff + t * r + zk] = zeros ? 0.f : v;
+    for (int m = 0; m < 2; ++m) {
+        if (m * 16 < rpad) {
+            float *wz = wb + zoff;  // [2T][rpad]
+            const int j = m * 16 + g;
+            if (col < Tp) {
+                wz[col * rpad + j] = zeros ? 0.f : zc[m][0];
+                wz[col * rpad + j + 8] = zeros ? 0.f : zc[m][2];
             }
-        }
-    }
-}
-
-// z contribution of one box: zacc[t] += sum over the box's 64 V rows i of
-// x[t][i] * V[i][k] for this lane's rank k = lane % RR; the lanes with the same
-// rank split the rows (RR = r rounded up to a power of two).  Fully unrolled
-// so that all shared-memory loads of a box are in flight together.
-template <int RR>
-__device__ __forceinline__ void z_box(const bf16 *__restrict__ vb, const bf16 *__restrict__ xr, int xsb, int r,
-                                      int T, bool lo, int lane, float (&zacc)[kStMaxT])
-{
-    constexpr int NG = 32 / RR, NI = kStBox / NG;
-    const int zk = lane % RR, zg = lane / RR;
-    if (zk >= r) return;
-    float vv[NI];
-#pragma unroll
-    for (int m = 0; m < NI; ++m) vv[m] = __bfloat162float(vb[(zg + NG * m) * r + zk]);
-#pragma unroll
-    for (int t = 0; t < kStMaxT; ++t) {
-        if (t < T) {
-            float acc = zacc[t];
-#pragma unroll
-            for (int m = 0; m < NI; ++m) {
-                const int i = zg + NG * m;
-                float xv = __bfloat162float(xr[t * xsb + i]);
-                if (lo) xv += __bfloat162float(xr[(T + t) * xsb + i]);
-                acc = fmaf(xv, vv[m], acc);
+            if (col + 1 < Tp) {
+                wz[(col + 1) * rpad + j] = zeros ? 0.f : zc[m][1];
+                wz[(col + 1) * rpad + j + 8] = zeros ? 0.f : zc[m][3];
             }
-            zacc[t] = acc;
         }
     }
 }
@@ -312,12 +291,6 @@ __device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap 
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
-__device__ __forceinline__ void bulk_g2s_u32(uint32_t dst, const void *src, unsigned bytes, uint64_t *bar)
-{
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
-                 "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
-}
 
 // ------------------------------------------------------------------ kernel
 // Start copying the record of phase ph_i of CTA c into its buffer (consumer
@@ -350,12 +323,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x, G = gridDim.x;
     const int T = a.T, r = a.r;
-    const int vblk = kStBox * r * 2, vblk16 = (vblk + 15) & ~15;
+    const int sbytes_stage = a.stage_bytes;
 
     // shared memory carve
     char *ring_w = smem;
-    char *ring_v = ring_w + (size_t)a.nst * kStBoxBytes;
-    uint64_t *full = reinterpret_cast<uint64_t *>(ring_v + (size_t)a.nst * vblk16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(ring_w + (size_t)a.nst * sbytes_stage);
     uint64_t *empty = full + a.nst;
     char *aux_us = reinterpret_cast<char *>(empty + a.nst);
     uint32_t *xst = reinterpret_cast<uint32_t *>(aux_us + (size_t)a.maxp * a.us_bytes);
@@ -381,8 +353,8 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
         // Per box only register arithmetic and the copies: the phase's fields
         // are read once per phase, box coordinates advance incrementally.
         if (lane != 0) return;
-        const unsigned sbytes = (unsigned)(kStBoxBytes + vblk);
-        const uint32_t w_base = smem_u32(ring_w), v_base = smem_u32(ring_v);
+        const unsigned sbytes = (unsigned)sbytes_stage;
+        const uint32_t w_base = smem_u32(ring_w);
         int s = 0;
         unsigned ph = 0;
         int issued = 0;
@@ -393,13 +365,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             if (b0 >= b1) continue;
             const bool gu = a.ph[phi].kind == kGU;
             const int KB = a.ph[phi].KB, bpr = a.ph[phi].bpr, nseg = a.ph[phi].nseg;
-            const CUtensorMap *map[3];
-            const bf16 *Vp[3];
+            const CUtensorMap *map[3], *vtm[3];
             int rt0[3];
 #pragma unroll
             for (int j = 0; j < 3; ++j) {
                 map[j] = a.ph[phi].seg[j].map;
-                Vp[j] = a.ph[phi].seg[j].V;
+                vtm[j] = a.ph[phi].seg[j].vtmap;
                 rt0[j] = j < nseg ? a.ph[phi].seg[j].rt0 : 0x7fffffff;
             }
             int rt = b0 / bpr, w = b0 - rt * bpr;
@@ -416,15 +387,16 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     row0 = (rt - (si == 2 ? rt0[2] : si == 1 ? rt0[1] : 0)) * kStBox;
                 }
                 const CUtensorMap *m = si == 2 ? map[2] : si == 1 ? map[1] : map[0];
-                const bf16 *V = si == 2 ? Vp[2] : si == 1 ? Vp[1] : Vp[0];
+                const CUtensorMap *vm = si == 2 ? vtm[2] : si == 1 ? vtm[1] : vtm[0];
                 if (flags[0] || !ring_wait_empty(&empty[s], ph ^ 1u, a.status)) {
                     ok = false;
                     break;
                 }
                 uint64_t *fb = &full[s];
                 mbar_expect_tx(fb, sbytes);
-                tma_load_2d_u32(w_base + (uint32_t)s * kStBoxBytes, m, kb * kStBox, row0, fb);
-                if (vblk) bulk_g2s_u32(v_base + (uint32_t)s * vblk16, V + (size_t)kb * kStBox * r, (unsigned)vblk, fb);
+                const uint32_t sdst = w_base + (uint32_t)s * (uint32_t)sbytes_stage;
+                tma_load_2d_u32(sdst, m, kb * kStBox, row0, fb);
+                if (a.rpad) tma_load_2d_u32(sdst + kStBoxBytes, vm, kb * kStBox, 0, fb);
                 ++issued;
                 if (++s == a.nst) {
                     s = 0;
@@ -453,7 +425,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     const int g = lane >> 2, t4 = lane & 3;
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8;  // ldmatrix row within a 16-row group
     const int lchunk = lane >> 4;
-    const int rr = a.rr > 0 ? a.rr : 1;
     int qbase = 0;  // CTA-local sequence number of the phase's first box
     fetch_rec(recbuf, a.rec, a.rec_ints, 0, G, c);
     cp_async_wait_all();
@@ -545,11 +516,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
 
             // ---- boxes: box j of the range goes to warp j % 8
             float cacc[4][4];
-            float zacc[kStMaxT];
+            float zc[2][4];
 #pragma unroll
             for (int m = 0; m < 4; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
 #pragma unroll
-            for (int t = 0; t < kStMaxT; ++t) zacc[t] = 0.f;
+            for (int m = 0; m < 2; ++m) zc[m][0] = zc[m][1] = zc[m][2] = zc[m][3] = 0.f;
+            const int rpad = a.rpad;
             int cur = -1;  // piece of the accumulators
             int pi = 0;
             float *wbw = wbuf + (size_t)warp * a.wb_floats;
@@ -557,13 +529,13 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             for (int j = warp; j < nbx; j += kWarps) {
                 while (pi + 1 < npc && j >= pcs[pi + 1].j0) ++pi;
                 if (pi != cur) {
-                    if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zacc, false, Tp, T, r, rr, lane);
+                    if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zc, false, Tp, rpad, lane);
                     for (int p = cur + 1; p < pi; ++p)
-                        flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zacc, true, Tp, T, r, rr, lane);
+                        flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zc, true, Tp, rpad, lane);
 #pragma unroll
                     for (int m = 0; m < 4; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
 #pragma unroll
-                    for (int t = 0; t < kStMaxT; ++t) zacc[t] = 0.f;
+                    for (int m = 0; m < 2; ++m) zc[m][0] = zc[m][1] = zc[m][2] = zc[m][3] = 0.f;
                     cur = pi;
                 }
                 const int q = qbase + j;
@@ -578,7 +550,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 }
                 int pos = pcs[pi].kb0 + (j - pcs[pi].j0) - kbs;
                 if (pos < 0) pos += KB;
-                const uint32_t sb = smem_u32(ring_w + (size_t)s * kStBoxBytes);
+                const uint32_t sb = smem_u32(ring_w + (size_t)s * sbytes_stage);
 #pragma unroll
                 for (int kin = 0; kin < 4; ++kin) {
                     uint32_t b0r = 0u, b1r = 0u;
@@ -595,37 +567,38 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                         ldmatrix_x4(af, sb + row * 128 + ((chunk ^ (row & 7)) << 4));
                         mma_16816(cacc[m], af, b0r, b1r);
                     }
-                }
-                if (r > 0) {
-                    const bf16 *vb = reinterpret_cast<const bf16 *>(ring_v + (size_t)s * vblk16);
-                    const bf16 *xr = xs + pos * kStBox;
-                    const bool lo = kind == kD;
-                    switch (rr) {
-                    case 1: z_box<1>(vb, xr, xsb, r, T, lo, lane, zacc); break;
-                    case 2: z_box<2>(vb, xr, xsb, r, T, lo, lane, zacc); break;
-                    case 4: z_box<4>(vb, xr, xsb, r, T, lo, lane, zacc); break;
-                    case 8: z_box<8>(vb, xr, xsb, r, T, lo, lane, zacc); break;
-                    case 16: z_box<16>(vb, xr, xsb, r, T, lo, lane, zacc); break;
-                    default: z_box<32>(vb, xr, xsb, r, T, lo, lane, zacc); break;
+                    // z = x V: the V^T rows (ranks) as M, the same token columns
+#pragma unroll
+                    for (int m = 0; m < 2; ++m) {
+                        if (m * 16 < rpad) {
+                            const int row = m * 16 + lrow;
+                            uint32_t af[4];
+                            ldmatrix_x4(af, sb + kStBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
+                            mma_16816(zc[m], af, b0r, b1r);
+                        }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
             qbase += nbx;
-            if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zacc, false, Tp, T, r, rr, lane);
+            if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zc, false, Tp, rpad, lane);
             for (int p = cur + 1; p < npc; ++p)
-                flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zacc, true, Tp, T, r, rr, lane);
+                flush_piece(wbw + p * wbp, a.wb_zoff, cacc, zc, true, Tp, rpad, lane);
             consumer_sync();
             if (flags[0]) break;  // every box loop has ended: all threads agree
 
             // ---- phase end: z per piece, then p = s * acc + U z per row
             for (int it = tid; it < npc * T * r; it += kThreads) {
                 const int p = it / (T * r), rem = it - p * T * r;
+                const int t = rem / r, j = rem - t * r;
                 float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w)
-                    sum += wbuf[((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff + rem];
+                for (int w = 0; w < kWarps; ++w) {
+                    const float *wz = wbuf + ((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff;
+                    sum += wz[t * a.rpad + j];
+                    if (kind == kD) sum += wz[(T + t) * a.rpad + j];
+                }
                 zsum[p * kStMaxT * kStMaxR + rem] = sum;
             }
             consumer_sync();
@@ -689,6 +662,23 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     cp_async_wait_all();
 }
 
+// V^T of every projection, padded with zero rows to rpad: VT[j][i] = V[i][j]
+// (j < r), 0 (r <= j < rpad).  One block row per projection, 256 columns i per
+// block; the writes of a row j are contiguous.
+struct VtJob {
+    const bf16 *V;  // [K, r]
+    bf16 *VT;       // [rpad, K]
+    int K;
+};
+
+__global__ void vt_kernel(const VtJob *__restrict__ jobs, int r, int rpad)
+{
+    const VtJob jb = jobs[blockIdx.y];
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= jb.K) return;
+    for (int j = 0; j < rpad; ++j) jb.VT[(size_t)j * jb.K + i] = j < r ? jb.V[(size_t)i * r + j] : __float2bfloat16_rn(0.f);
+}
+
 // ------------------------------------------------------------------- host
 struct StackPlan {
     int device = -1;
@@ -697,6 +687,8 @@ struct StackPlan {
     unsigned epoch = 0;
     std::vector<StArgs> chunks;           // one launch per chunk of at most 24 layers
     std::vector<const bf16 *> chunk_x;    // input of each chunk (null: the caller's x)
+    const VtJob *vt_jobs = nullptr;       // V^T jobs (device), run before each step
+    int n_vt = 0, vt_maxk = 0, rpad = 0;
     void *dmem = nullptr;  // tensor maps, partial tables, partial words
 };
 
@@ -818,7 +810,6 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
                 P.seg[j].out = (int)h.proj[j]->out;
                 P.seg[j].s = h.proj[j]->s;
                 P.seg[j].U = static_cast<const bf16 *>(h.proj[j]->U);
-                P.seg[j].V = static_cast<const bf16 *>(h.proj[j]->V);
                 P.seg[j].nrt = cdiv_i(h.proj[j]->out, 64);
                 P.seg[j].rt0 = (k == kGU) ? 0 : rt;
                 if (k != kGU) rt += P.seg[j].nrt;
@@ -942,16 +933,15 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     };
 
     // ---- shared memory
-    int rr = 1;
-    while (rr < r) rr <<= 1;
-    const int vblk16 = ((int)(64 * r * 2) + 15) & ~15;
+    const int rpad = r == 0 ? 0 : (r <= 16 ? 16 : 32);
     const int us_bytes = ((int)(64 * r * 2) + 16 + 15) / 16 * 16 + (64 * 4 + 16 + 15) / 16 * 16;
     int xs32 = (nkmax * 64 + 8) / 2;  // row stride (u32); 4 mod 32 keeps the B-operand reads conflict-free
     xs32 = (xs32 + 31) / 32 * 32 + 4;
-    const int wb_floats = 2 * (int)T * 64 + (int)T * (int)(r > 0 ? r : 1);
+    const int wb_floats = 2 * (int)T * 64 + 2 * (int)T * (rpad > 0 ? rpad : 1);
     const int fixed = 1024 + maxp * us_bytes + 2 * (int)T * xs32 * 4 + maxp * kWarps * wb_floats * 4 +
                       maxp * kStMaxT * kStMaxR * 4 + 2 * rec_ints * 4 + 16 + 64;
-    const int per_stage = kStBoxBytes + vblk16 + 16;
+    const int stage_bytes = kStBoxBytes + rpad * 128;  // W0 box + V^T box, 1024-byte multiple
+    const int per_stage = stage_bytes + 16;
     int nst = (di->max_smem_optin - fixed) / per_stage;
     if (nst > 32) nst = 32;
     if (nst < 8)
@@ -967,6 +957,8 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
         return o;
     };
     const size_t o_maps = take(sizeof(CUtensorMap) * 7 * L, 128);
+    const size_t o_vtmaps = take(sizeof(CUtensorMap) * 7 * L, 128);
+    const size_t o_jobs = take(sizeof(VtJob) * 7 * L, 16);
     std::vector<size_t> o_np(4 * L), o_s0(4 * L), o_part(4 * L);
     for (size_t i = 0; i < hp.size(); ++i) {
         o_np[i] = take(sizeof(int) * hp[i].P.nrt, 16);
@@ -974,6 +966,10 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     }
     const size_t o_rec = take(sizeof(int) * (size_t)rec_ints * 4 * L * G, 256);
     const size_t o_tables_end = take(0, 256);
+    const int64_t kin[7] = {hidden, hidden, hidden, qd, hidden, hidden, inter};
+    std::vector<size_t> o_vt(7 * L);
+    for (int64_t l = 0; l < L; ++l)
+        for (int j = 0; j < 7; ++j) o_vt[7 * l + j] = take((size_t)rpad * kin[j] * 2, 256);
     for (size_t i = 0; i < hp.size(); ++i)
         o_part[i] = take(sizeof(unsigned long long) * (size_t)hp[i].nslots * hp[i].P.nsub * T * 64, 256);
     const size_t total = off;
@@ -999,13 +995,31 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
             }
         }
     }
+    // V^T buffers, their tensor maps and the transpose jobs
+    CUtensorMap *hvt = reinterpret_cast<CUtensorMap *>(host.data() + o_vtmaps);
+    VtJob *hjobs = reinterpret_cast<VtJob *>(host.data() + o_jobs);
+    for (int64_t l = 0; l < L && rpad > 0; ++l) {
+        const wl_proj *pj[7] = {&layers[l].q, &layers[l].k, &layers[l].v, &layers[l].o,
+                                &layers[l].gate, &layers[l].up, &layers[l].down};
+        for (int j = 0; j < 7; ++j) {
+            bf16 *vt = reinterpret_cast<bf16 *>(base + o_vt[7 * l + j]);
+            st = tmap_2d_bf16(vt, kin[j], rpad, kin[j], 64, rpad, &hvt[7 * l + j]);
+            if (st != WL_OK) {
+                cudaFree(dmem);
+                return st;
+            }
+            hjobs[7 * l + j] = VtJob{static_cast<const bf16 *>(pj[j]->V), vt, (int)kin[j]};
+        }
+    }
     for (size_t i = 0; i < hp.size(); ++i) {
         HostPhase &h = hp[i];
         const int64_t l = (int64_t)i / 4;
         const int k = (int)(i % 4);
         const int mj[4][3] = {{0, 1, 2}, {3, -1, -1}, {4, 5, -1}, {6, -1, -1}};
-        for (int j = 0; j < h.P.nseg; ++j)
+        for (int j = 0; j < h.P.nseg; ++j) {
             h.P.seg[j].map = reinterpret_cast<const CUtensorMap *>(base + o_maps) + 7 * l + mj[k][j];
+            h.P.seg[j].vtmap = rpad ? reinterpret_cast<const CUtensorMap *>(base + o_vtmaps) + 7 * l + mj[k][j] : nullptr;
+        }
         memcpy(host.data() + o_np[i], h.np.data(), sizeof(int) * h.P.nrt);
         memcpy(host.data() + o_s0[i], h.slot0.data(), sizeof(int) * h.P.nrt);
         h.P.np = reinterpret_cast<const int *>(base + o_np[i]);
@@ -1041,13 +1055,14 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     memset(&a, 0, sizeof(a));
     a.T = (int)T;
     a.r = (int)r;
-    a.rr = rr;
     a.nst = nst;
     a.maxp = maxp;
     a.xs32 = xs32;
     a.us_bytes = us_bytes;
     a.wb_floats = wb_floats;
     a.wb_zoff = 2 * (int)T * 64;
+    a.rpad = rpad;
+    a.stage_bytes = stage_bytes;
     a.maxnk = nkmax;
     a.rec_ints = rec_ints;
     a.status = di->status;
@@ -1078,6 +1093,10 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
         pl.chunk_x.push_back(l0 == 0 ? nullptr : static_cast<const bf16 *>(outs[l0 - 1].ym));
     }
     pl.dmem = dmem;
+    pl.rpad = rpad;
+    pl.n_vt = rpad ? (int)(7 * L) : 0;
+    pl.vt_maxk = (int)std::max(hidden, std::max(qd, inter));
+    pl.vt_jobs = reinterpret_cast<const VtJob *>(base + o_jobs);
 
     wl_stack_s *h = new (std::nothrow) wl_stack_s;
     if (!h) {
@@ -1105,6 +1124,13 @@ extern "C" wl_status wl_stack_decode(wl_stack stk, const void *x, void *stream)
         // epochs 1 .. 2^32-1; 0 marks words never written
         if (++pl.epoch == 0) pl.epoch = 1;
         epoch = pl.epoch;
+    }
+    if (pl.n_vt > 0) {
+        // V^T of this step's V (read now, so later changes to V are seen)
+        dim3 grid((unsigned)((pl.vt_maxk + 255) / 256), (unsigned)pl.n_vt);
+        vt_kernel<<<grid, 256, 0, static_cast<cudaStream_t>(stream)>>>(pl.vt_jobs, pl.r, pl.rpad);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "wl_stack_decode: V^T launch");
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.G);
