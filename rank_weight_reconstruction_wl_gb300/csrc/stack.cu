@@ -332,7 +332,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
     char *aux_us = reinterpret_cast<char *>(empty + a.nst);
     uint32_t *xst = reinterpret_cast<uint32_t *>(aux_us + (size_t)a.maxp * a.us_bytes);
     float *wbuf = reinterpret_cast<float *>(xst + (size_t)(2 * T) * a.xs32);  // [maxp][8][wb_floats]
-    float *zsum = wbuf + (size_t)a.maxp * kWarps * a.wb_floats;                     // [maxp][T][r]
+    float *zsum = wbuf + (size_t)a.maxp * kWarps * a.wb_floats;                     // [maxp][T][r] (r > 8)
     int *recbuf = reinterpret_cast<int *>(zsum + a.maxp * kStMaxT * kStMaxR);  // 2 x rec_ints
     // [0] consumers gave up (written only by consumers; read for control
     // right after a consumer barrier), [2] producer gave up
@@ -588,20 +588,25 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             consumer_sync();
             if (flags[0]) break;  // every box loop has ended: all threads agree
 
-            // ---- phase end: z per piece, then p = s * acc + U z per row
-            for (int it = tid; it < npc * T * r; it += kThreads) {
-                const int p = it / (T * r), rem = it - p * T * r;
-                const int t = rem / r, j = rem - t * r;
-                float sum = 0.f;
+            // ---- phase end: p = s * acc + U z per row, the warps' sums added in
+            // warp order.  Small r: z over the warps inside the rank loop; larger
+            // r: z summed once per (piece, token, rank) first.
+            const bool zfused = r <= 8;
+            if (!zfused) {
+                for (int it = tid; it < npc * T * r; it += kThreads) {
+                    const int p = it / (T * r), rem = it - p * T * r;
+                    const int t = rem / r, j = rem - t * r;
+                    float sum = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
-                    const float *wz = wbuf + ((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff;
-                    sum += wz[t * a.rpad + j];
-                    if (kind == kD) sum += wz[(T + t) * a.rpad + j];
+                    for (int w = 0; w < kWarps; ++w) {
+                        const float *wz = wbuf + ((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff;
+                        sum += wz[t * a.rpad + j];
+                        if (kind == kD) sum += wz[(T + t) * a.rpad + j];
+                    }
+                    zsum[p * kStMaxT * kStMaxR + rem] = sum;
                 }
-                zsum[p * kStMaxT * kStMaxR + rem] = sum;
+                consumer_sync();
             }
-            consumer_sync();
             for (int it = tid; it < npc * T * kStBox; it += kThreads) {
                 const int p = it / (T * kStBox), rem = it - p * T * kStBox;
                 const int t = rem >> 6, row = rem & 63;
@@ -623,8 +628,21 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     const float *sr = reinterpret_cast<const float *>(
                         us + ((kStBox * r * 2 + 16 + 15) & ~15) + (reinterpret_cast<uintptr_t>(sg.s + pc.row0) & 15));
                     v = sr[row] * acc;
+                    const float *wz0 = wbuf + (size_t)p * kWarps * a.wb_floats + a.wb_zoff;
                     const float *zp = zsum + p * kStMaxT * kStMaxR + t * r;
-                    for (int k = 0; k < r; ++k) v = fmaf(__bfloat162float(Ur[row * r + k]), zp[k], v);
+                    for (int k = 0; k < r; ++k) {
+                        float z = 0.f;
+                        if (zfused) {
+#pragma unroll
+                            for (int w = 0; w < kWarps; ++w) {
+                                z += wz0[(size_t)w * a.wb_floats + t * a.rpad + k];
+                                if (kind == kD) z += wz0[(size_t)w * a.wb_floats + (T + t) * a.rpad + k];
+                            }
+                        } else {
+                            z = zp[k];
+                        }
+                        v = fmaf(__bfloat162float(Ur[row * r + k]), z, v);
+                    }
                 }
                 unsigned long long *sp = P.part + (size_t)pc.slot * P.nsub * T * kStBox;
                 st_word(sp + ((size_t)pc.sub * T + t) * kStBox + row, v, a.epoch);
@@ -637,10 +655,11 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             }
         }
 
-        // ---- outputs no phase reads (k, v; the last layer's): assigned row tiles
+        // ---- outputs no phase reads (k, v; the last layer's): assigned row
+        // tiles, counted from the last CTA (O leaves the upper half idle)
         if (P.xw_n > 0) {
             const StPhase &X = a.ph[P.xw_ph];
-            for (int w = c; w < P.xw_n; w += G) {
+            for (int w = G - 1 - c; w < P.xw_n; w += G) {
                 const int rt = P.xw_rt0 + w;
                 int si = 0;
                 while (si + 1 < X.nseg && rt >= X.seg[si + 1].rt0) ++si;
