@@ -157,39 +157,8 @@ __device__ __forceinline__ unsigned long long ld_word(const unsigned long long *
 __device__ __forceinline__ float word_val(unsigned long long w) { return __uint_as_float((unsigned)w); }
 __device__ __forceinline__ bool word_ok(unsigned long long w, unsigned epoch) { return (unsigned)(w >> 32) == epoch; }
 
-// Sums of partial words: elements i0..i0+3 of token t, part `sub` of a row
-// tile of phase Q (its n partials start at slot0), polled until every word carries the epoch (bounded).  Sums
-// run in slot order.  On giving up the status word is set and *ok cleared.
-__device__ __forceinline__ float4 sum4(const StPhase &Q, int n, int slot0, int sub, int t, int i0, int T,
-                                       unsigned epoch, bool *ok_out, unsigned *status)
-{
-    const size_t stride = (size_t)Q.nsub * T * kStBox;
-    const unsigned long long *p = Q.part + ((size_t)slot0 * Q.nsub + sub) * T * kStBox + t * kStBox + i0;
-    uint64_t t0 = 0;
-    for (;;) {
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
-        bool ok = true;
-#pragma unroll 4
-        for (int j = 0; j < n; ++j) {
-            const ulonglong2 a = ld_words2(p + j * stride);
-            const ulonglong2 b = ld_words2(p + j * stride + 2);
-            ok = ok && word_ok(a.x, epoch) && word_ok(a.y, epoch) && word_ok(b.x, epoch) && word_ok(b.y, epoch);
-            s[0] += word_val(a.x);
-            s[1] += word_val(a.y);
-            s[2] += word_val(b.x);
-            s[3] += word_val(b.y);
-        }
-        if (ok) return make_float4(s[0], s[1], s[2], s[3]);
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
-            atomicOr(status, kStatusTimeout | kWaitExchange);
-            *ok_out = false;
-            return make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    }
-}
-
-// One element (part 0) of a row tile of phase Q, polled like sum4.
+// One element (part 0) of a row tile of phase Q (n partials from slot0),
+// polled until it carries the epoch (bounded).
 __device__ __forceinline__ float sum1(const StPhase &Q, int n, int slot0, int t, int i, int T, unsigned epoch,
                                       bool *ok_out, unsigned *status)
 {
@@ -290,6 +259,99 @@ __device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap 
         " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Sums of partial words for NQ groups of 4 rows (i0 ..) of token t and NS
+// parts of a row tile of phase Q (n partials from slot0): every load of every
+// slot is issued before the epochs are checked, so a ready input costs one
+// round trip.  Sums run in slot order.  false: gave up (status set).
+template <int NQ, int NS>
+__device__ __forceinline__ bool sumq(const StPhase &Q, int n, int slot0, int t, int i0, int T, unsigned epoch,
+                                     float (&out)[NS][NQ * 4], unsigned *status)
+{
+    const size_t stride = (size_t)Q.nsub * T * kStBox;
+    const unsigned long long *base = Q.part + (size_t)slot0 * Q.nsub * T * kStBox + t * kStBox + i0;
+    uint64_t t0 = 0;
+    for (;;) {
+        float acc[NS][NQ * 4];
+#pragma unroll
+        for (int ps = 0; ps < NS; ++ps)
+#pragma unroll
+            for (int e = 0; e < NQ * 4; ++e) acc[ps][e] = 0.f;
+        bool ok = true;
+#pragma unroll 2
+        for (int j = 0; j < n; ++j) {
+#pragma unroll
+            for (int ps = 0; ps < NS; ++ps)
+#pragma unroll
+                for (int q = 0; q < NQ; ++q) {
+                    const unsigned long long *pp = base + j * stride + (size_t)ps * T * kStBox + 4 * q;
+                    const ulonglong2 u = ld_words2(pp), v = ld_words2(pp + 2);
+                    ok = ok && word_ok(u.x, epoch) && word_ok(u.y, epoch) && word_ok(v.x, epoch) && word_ok(v.y, epoch);
+                    acc[ps][4 * q] += word_val(u.x);
+                    acc[ps][4 * q + 1] += word_val(u.y);
+                    acc[ps][4 * q + 2] += word_val(v.x);
+                    acc[ps][4 * q + 3] += word_val(v.y);
+                }
+        }
+        if (ok) {
+#pragma unroll
+            for (int ps = 0; ps < NS; ++ps)
+#pragma unroll
+                for (int e = 0; e < NQ * 4; ++e) out[ps][e] = acc[ps][e];
+            return true;
+        }
+        if (t0 == 0) t0 = globaltimer_ns();
+        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            atomicOr(status, kStatusTimeout | kWaitExchange);
+            return false;
+        }
+    }
+}
+
+// The phase input from the previous phase's partials: items of NQ groups of 4
+// elements of one token of one staged block (consumer threads).  D forms
+// h = gelu(g) u from the gate and up parts and stages it as bf16 hi + lo;
+// the others round to bf16, and the owner of box kb of the first row tile
+// stores block kb to the previous phase's output.  false: a wait gave up.
+template <int NQ>
+__device__ __forceinline__ bool gather_items(const StPhase &P, const StPhase &Q, const int *gnp, const int *gs0,
+                                             int kbs, int nk, int T, int b0, int b1, bf16 *xs, int xsb,
+                                             unsigned epoch, unsigned *status)
+{
+    constexpr int per_tok = 16 / NQ;  // items per token and block
+    const int KB = P.KB;
+    for (int it = threadIdx.x; it < nk * T * per_tok; it += kThreads) {
+        const int pos = it / (T * per_tok);
+        const int rem = it - pos * T * per_tok;
+        const int t = rem / per_tok, i0 = (rem % per_tok) * 4 * NQ;
+        int kb = kbs + pos;
+        if (kb >= KB) kb -= KB;
+        const int col = pos * kStBox + i0;
+        const int qn = gnp[pos], qs = gs0[pos];
+        if (P.kind == kD) {
+            float gu[2][NQ * 4];
+            if (!sumq<NQ, 2>(Q, qn, qs, t, i0, T, epoch, gu, status)) return false;
+#pragma unroll
+            for (int e = 0; e < NQ * 4; ++e) {
+                const float hv = gelu_tanh_f32(gu[0][e]) * gu[1][e];
+                const bf16 hi = __float2bfloat16_rn(hv);
+                xs[t * xsb + col + e] = hi;
+                xs[(T + t) * xsb + col + e] = __float2bfloat16_rn(hv - __bfloat162float(hi));
+            }
+        } else {
+            float v[1][NQ * 4];
+            if (!sumq<NQ, 1>(Q, qn, qs, t, i0, T, epoch, v, status)) return false;
+            const bool wr = P.wy && kb >= b0 && kb < b1;
+#pragma unroll
+            for (int e = 0; e < NQ * 4; ++e) {
+                const bf16 b = __float2bfloat16_rn(v[0][e]);
+                xs[t * xsb + col + e] = b;
+                if (wr) P.wy[(size_t)t * P.K + (size_t)kb * kStBox + i0 + e] = b;
+            }
+        }
+    }
+    return true;
 }
 
 // ------------------------------------------------------------------ kernel
@@ -458,48 +520,12 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             const int xsb = 2 * a.xs32;  // x stage row stride (bf16)
             if (P.prev >= 0) {
                 const StPhase &Q = a.ph[P.prev];
-                // groups of 4 elements of one token of one input block
-                for (int it = tid; it < nk * T * 16; it += kThreads) {
-                    const int pos = it / (T * 16);
-                    const int rem = it - pos * T * 16;
-                    const int t = rem >> 4, i0 = (rem & 15) * 4;
-                    int kb = kbs + pos;
-                    if (kb >= KB) kb -= KB;
-                    const int col = pos * kStBox + i0;
-                    bool ok = true;
-                    const int qn = gnp[pos], qs = gs0[pos];
-                    if (kind == kD) {
-                        const float4 g4 = sum4(Q, qn, qs, 0, t, i0, T, a.epoch, &ok, a.status);
-                        const float4 u4 = ok ? sum4(Q, qn, qs, 1, t, i0, T, a.epoch, &ok, a.status)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-                        if (!ok) {
-                            flags[0] = 1;
-                            break;
-                        }
-                        const float gv[4] = {g4.x, g4.y, g4.z, g4.w}, uv[4] = {u4.x, u4.y, u4.z, u4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float hv = gelu_tanh_f32(gv[e]) * uv[e];
-                            const bf16 hi = __float2bfloat16_rn(hv);
-                            xs[t * xsb + col + e] = hi;
-                            xs[(T + t) * xsb + col + e] = __float2bfloat16_rn(hv - __bfloat162float(hi));
-                        }
-                    } else {
-                        const float4 v4 = sum4(Q, qn, qs, 0, t, i0, T, a.epoch, &ok, a.status);
-                        if (!ok) {
-                            flags[0] = 1;
-                            break;
-                        }
-                        const float v[4] = {v4.x, v4.y, v4.z, v4.w};
-                        const bool wr = P.wy && kb >= b0 && kb < b1;
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const bf16 b = __float2bfloat16_rn(v[e]);
-                            xs[t * xsb + col + e] = b;
-                            if (wr) P.wy[(size_t)t * P.K + (size_t)kb * kStBox + i0 + e] = b;
-                        }
-                    }
-                }
+                // one item per thread where possible (a ready input then costs
+                // one round trip): 8 elements per item when 4 would not fit
+                const bool ok = (nk * T * 16 > kThreads)
+                                    ? gather_items<2>(P, Q, gnp, gs0, kbs, nk, T, b0, b1, xs, xsb, a.epoch, a.status)
+                                    : gather_items<1>(P, Q, gnp, gs0, kbs, nk, T, b0, b1, xs, xsb, a.epoch, a.status);
+                if (!ok) flags[0] = 1;
             } else {
                 for (int it = tid; it < nk * T * kStBox; it += kThreads) {
                     const int pos = it / (T * kStBox);
