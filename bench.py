@@ -408,55 +408,54 @@ def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
     ym = torch.empty(T, SHAPES["hidden"], **z)
     ws = wl.mlp_workspace(T, SHAPES["hidden"], SHAPES["inter"], r, torch.bfloat16, dev)
     st = torch.cuda.Stream(dev)
-    ev = {k: [] for k in ("qkv", "o", "mlp")}
+    # The layer's launches are captured once as CUDA graphs and replayed, so
+    # that the timings are device time (no host launch overhead inside).
+    parts = {"qkv": lambda th: wl.wl_qkv_fused(x, th.q, th.k, th.v, outs=(yq, yk, yv), stream=st),
+             "o": lambda th: wl.wl_linear(yq, th.o.W0, th.o.s, th.o.U, th.o.V, y=yo, stream=st),
+             "mlp": lambda th: wl.wl_mlp_geglu_fused(yo, th.gate, th.up, th.down, y=ym, workspace=ws, stream=st)}
 
-    def layer(th, timed):
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        if timed:
-            e[0].record(st)
-        wl.wl_qkv_fused(x, th.q, th.k, th.v, outs=(yq, yk, yv), stream=st)
-        if timed:
-            e[1].record(st)
-        wl.wl_linear(yq, th.o.W0, th.o.s, th.o.U, th.o.V, y=yo, stream=st)
-        if timed:
-            e[2].record(st)
-        wl.wl_mlp_geglu_fused(yo, th.gate, th.up, th.down, y=ym, workspace=ws, stream=st)
-        if timed:
-            e[3].record(st)
-            ev["qkv"].append((e[0], e[1]))
-            ev["o"].append((e[1], e[2]))
-            ev["mlp"].append((e[2], e[3]))
-
-    with torch.cuda.stream(st):
-        for th in layers:
-            layer(th, False)
-        st.synchronize()
-        t0 = torch.cuda.Event(enable_timing=True)
-        t1 = torch.cuda.Event(enable_timing=True)
-        t0.record(st)
-        for _ in range(reps):
+    def capture(fns):
+        with torch.cuda.stream(st):
             for th in layers:
-                layer(th, False)
-        t1.record(st)
-        st.synchronize()
-        for th in layers:
-            layer(th, True)
-        st.synchronize()
-    ms = t0.elapsed_time(t1) / (reps * nlayers)
+                for f in fns:
+                    f(th)
+            st.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=st):
+                for _ in range(reps):
+                    for th in layers:
+                        for f in fns:
+                            f(th)
+        return g
+
+    def time_graph(g):
+        with torch.cuda.stream(st):
+            g.replay()
+            st.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(st)
+            g.replay()
+            a1.record(st)
+            st.synchronize()
+        return a0.elapsed_time(a1) / (reps * nlayers)
+
+    ms = time_graph(capture(list(parts.values())))
+    part_ms = {k: time_graph(capture([f])) for k, f in parts.items()}
     flops = layer_flops(SHAPES, T, r)
     h, q, kv, i = SHAPES["hidden"], SHAPES["q"], SHAPES["kv"], SHAPES["inter"]
     part_flops = {"qkv": 2 * T * (h * (q + 2 * kv) + r * 3 * h + r * (q + 2 * kv)),
                   "o": 2 * T * (q * h + r * (q + h)),
                   "mlp": 2 * T * (3 * h * i + r * 3 * (h + i))}
-    parts = {}
-    for k, pairs in ev.items():
-        pms = statistics.mean(a.elapsed_time(b) for a, b in pairs)
-        parts[k] = {"us": round(pms * 1e3, 2), "tflops": round(part_flops[k] / (pms * 1e-3) / 1e12, 1)}
+    out_parts = {}
+    for k, pms in part_ms.items():
+        out_parts[k] = {"us": round(pms * 1e3, 2), "tflops": round(part_flops[k] / (pms * 1e-3) / 1e12, 1)}
     _, bf16_peak, kind = load_peaks()
     tf = flops / (ms * 1e-3) / 1e12
     return {"T": T, "r": r, "ms_per_layer": round(ms, 4), "tflops": round(tf, 1),
             "frac_of_bf16_peak": round(tf / bf16_peak, 4), "peak_tflops": bf16_peak, "peak_kind": kind,
-            "layer_gflop": round(flops / 1e9, 2), "parts": parts,
+            "layer_gflop": round(flops / 1e9, 2), "parts": out_parts,
+            "timing": "CUDA graph replay of the layer's launches (device time)",
             "l2": f"{nlayers} weight sets rotated (larger than L2)"}
 
 

@@ -508,6 +508,8 @@ static std::unordered_map<int, int> g_pf_attr;
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
                          int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st)
 {
+    if (prefill_tiles_applicable(Ktot, r, ydt, false))
+        return launch_prefill_tiles(x, proj, nproj, false, y, 0, T, in, Ktot, kmod, r, ydt, 0, 0, st);
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
     if (!di) return s;
@@ -646,6 +648,19 @@ wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &
     if (ws_bytes < prefill_mlp_workspace_bytes(T, inter, ydt))
         return fail(WL_ERR_WORKSPACE, "MLP workspace too small for %lld tokens", (long long)T);
     char *w = static_cast<char *>(ws);
+    if (prefill_tiles_applicable(hidden, r, ydt, true)) {
+        // gate and up in one persistent launch whose epilogue forms h, then down
+        const int64_t kmod = (inter + kBKp - 1) / kBKp * kBKp;
+        const int64_t ld = ydt == WL_OUT_F32 ? 2 * kmod : kmod;
+        bf16 *hb = reinterpret_cast<bf16 *>(w + 256);
+        const wl_proj gu[2] = {gate, up};
+        void *yh[1] = {hb};
+        wl_status s = launch_prefill_tiles(x, gu, 2, true, yh, ld, T, hidden, hidden, hidden, r, ydt, kmod,
+                                           ydt == WL_OUT_F32 ? kmod : 0, st);
+        if (s != WL_OK) return s;
+        void *yd[1] = {y};
+        return launch_prefill(hb, &down, 1, yd, T, inter, ld, kmod, r, ydt, st);
+    }
     float *g = reinterpret_cast<float *>(w + 256);
     float *u = reinterpret_cast<float *>(w + 256 + al256(T * inter * 4));
     bf16 *hb = reinterpret_cast<bf16 *>(w + 256 + 2 * al256(T * inter * 4));

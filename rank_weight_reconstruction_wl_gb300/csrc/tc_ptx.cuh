@@ -68,4 +68,35 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float v[16])
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 8 consecutive fp32 columns of this thread's TMEM lane, without waiting:
+// the registers are valid only after tmem_wait_ld8() on them.
+__device__ __forceinline__ void tmem_ld8_nw(uint32_t taddr, uint32_t r[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+// Wait for this thread's outstanding TMEM loads.  The registers of one load
+// are operands, so that the compiler cannot read them before the wait; after
+// a first wait, further calls for other loads cost nothing.
+__device__ __forceinline__ void tmem_wait_ld8(uint32_t r[8])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
+}
+
+// Store 8 consecutive fp32 columns of this thread's TMEM lane; complete after
+// tmem_wait_st().
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const float v[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+                 "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+                 "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+                 "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 }  // namespace wl

@@ -26,11 +26,11 @@ static std::mutex g_tmap_mu;
 struct TmapKey {
     uintptr_t base;
     int64_t inner, outer, ld;
-    int box_inner, box_outer;
+    int box_inner, box_outer, swz;
     bool operator==(const TmapKey &o) const
     {
         return base == o.base && inner == o.inner && outer == o.outer && ld == o.ld &&
-               box_inner == o.box_inner && box_outer == o.box_outer;
+               box_inner == o.box_inner && box_outer == o.box_outer && swz == o.swz;
     }
 };
 struct TmapKeyHash {
@@ -39,7 +39,8 @@ struct TmapKeyHash {
         uint64_t h = k.base * 0x9E3779B97F4A7C15ull;
         h ^= (uint64_t)k.inner + 0x632BE59BD9B4E019ull + (h << 6) + (h >> 2);
         h ^= (uint64_t)k.outer + 0x85EBCA77C2B2AE63ull + (h << 6) + (h >> 2);
-        h ^= (uint64_t)k.ld * 31 + (uint64_t)(k.box_inner * 1024 + k.box_outer) + (h << 6) + (h >> 2);
+        h ^= (uint64_t)k.ld * 31 + (uint64_t)(k.box_inner * 1024 + k.box_outer) * 8 + (uint64_t)k.swz +
+             (h << 6) + (h >> 2);
         return (size_t)h;
     }
 };
@@ -48,6 +49,19 @@ static std::unordered_map<TmapKey, CUtensorMap, TmapKeyHash> g_tmaps;
 wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
                        int box_inner, int box_outer, CUtensorMap *out)
 {
+    return tmap_2d_bf16_swz(base, inner, outer, ld_elems, box_inner, box_outer, 128, out);
+}
+
+wl_status tmap_2d_bf16_swz(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
+                           int box_inner, int box_outer, int swizzle_bytes, CUtensorMap *out)
+{
+    CUtensorMapSwizzle sw;
+    switch (swizzle_bytes) {
+    case 32: sw = CU_TENSOR_MAP_SWIZZLE_32B; break;
+    case 64: sw = CU_TENSOR_MAP_SWIZZLE_64B; break;
+    case 128: sw = CU_TENSOR_MAP_SWIZZLE_128B; break;
+    default: return fail(WL_ERR_UNSUPPORTED, "tensor map: swizzle of %d bytes", swizzle_bytes);
+    }
     std::lock_guard<std::mutex> lk(g_tmap_mu);
     if (!g_encode) {
         cudaDriverEntryPointQueryResult q;
@@ -58,7 +72,7 @@ wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t l
             return fail(WL_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
         g_encode = reinterpret_cast<encode_tiled_fn>(fn);
     }
-    const TmapKey key{reinterpret_cast<uintptr_t>(base), inner, outer, ld_elems, box_inner, box_outer};
+    const TmapKey key{reinterpret_cast<uintptr_t>(base), inner, outer, ld_elems, box_inner, box_outer, swizzle_bytes};
     auto it = g_tmaps.find(key);
     if (it != g_tmaps.end()) {
         *out = it->second;
@@ -72,7 +86,7 @@ wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t l
     const cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS)
         return fail(WL_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d) for a [%lld, %lld] matrix", (int)r,

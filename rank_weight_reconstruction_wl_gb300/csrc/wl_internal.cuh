@@ -79,6 +79,10 @@ const DeviceInfo *device_info(wl_status *st);
 // ld_elems, box [box_outer, box_inner], 128-byte swizzle (cached).
 wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
                        int box_inner, int box_outer, CUtensorMap *out);
+// The same with a swizzle span of 32, 64 or 128 bytes (box_inner * 2 bytes
+// at most the span).
+wl_status tmap_2d_bf16_swz(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
+                           int box_inner, int box_outer, int swizzle_bytes, CUtensorMap *out);
 
 // Record a message for wl_last_error() and return the status.
 wl_status fail(wl_status st, const char *fmt, ...);
@@ -99,6 +103,15 @@ size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r);
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
                          int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st);
 size_t prefill_mlp_workspace_bytes(int64_t T, int64_t inter, int ydt);
+// Persistent tensor-core kernel (double-buffered TMEM accumulators); the
+// split-K kernel above takes what it does not (long K chains with fp32
+// outputs, larger ranks).  pair: proj[0] = gate, proj[1] = up, and y[0] is h
+// (row stride ldy) = gelu_tanh(gate) * up, hw columns per part, the bf16
+// rounding remainder at column hlo (0: none).
+bool prefill_tiles_applicable(int64_t Ktot, int64_t r, int ydt, bool pair);
+wl_status launch_prefill_tiles(const bf16 *x, const wl_proj *proj, int nproj, bool pair, void *const *y,
+                               int64_t ldy, int64_t T, int64_t in, int64_t Ktot, int64_t kmod, int64_t r,
+                               int ydt, int64_t hw, int64_t hlo, cudaStream_t st);
 wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up, const wl_proj &down,
                              void *y, int64_t T, int64_t hidden, int64_t inter, int64_t r, void *ws,
                              size_t ws_bytes, int ydt, cudaStream_t st);
