@@ -483,6 +483,8 @@ def main():
     ap.add_argument("--no-compare", action="store_true", help="skip timing the per-projection graph engine")
     ap.add_argument("--engine", default="auto", choices=["auto", "stack", "graph"],
                     help="stack kernel (one launch per 24 layers) or per-projection CUDA graph")
+    ap.add_argument("--only-prefill", action="store_true",
+                    help="run only the T=2048 prefill layer measurement (for profiling)")
     ap.add_argument("--layers", type=int, default=L_LAYERS,
                     help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()
@@ -494,6 +496,13 @@ def main():
         if args.steps > 20:
             args.steps = 20
         run_reference(args)
+        return
+    if args.only_prefill:
+        import torch
+
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        print(json.dumps({"prefill_T2048": measure_prefill(dev, nlayers=min(args.layers, 4), reps=1)}))
         return
     run_wl(args)
 

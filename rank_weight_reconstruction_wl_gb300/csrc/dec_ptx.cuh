@@ -57,13 +57,13 @@ __device__ __forceinline__ bool mbar_test_cluster(uint64_t *bar, unsigned parity
     return ok != 0;
 }
 
-// Bounded waits: false after kWaitLimitNs (the status word is then set).
+// Bounded waits: false after kWaitLimitCycles (the status word is then set).
 static __device__ __noinline__ bool mbar_wait(uint64_t *bar, unsigned parity, unsigned *status, unsigned site)
 {
     if (mbar_test(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = wait_clock();
     while (!mbar_test(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (wait_clock() - t0 > kWaitLimitCycles) {
             atomicOr(status, kStatusTimeout | site);
             return false;
         }
@@ -74,9 +74,9 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, unsigned parity, un
 static __device__ __noinline__ bool mbar_wait_cluster(uint64_t *bar, unsigned parity, unsigned *status)
 {
     if (mbar_test_cluster(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = wait_clock();
     while (!mbar_test_cluster(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (wait_clock() - t0 > kWaitLimitCycles) {
             atomicOr(status, kStatusTimeout | kWaitExchange);
             return false;
         }

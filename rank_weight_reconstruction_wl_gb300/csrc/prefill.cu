@@ -68,9 +68,9 @@ __device__ __forceinline__ bool pf_test(uint64_t *bar, unsigned parity)
 __device__ __noinline__ bool pf_wait(uint64_t *bar, unsigned parity, unsigned *status, unsigned site)
 {
     if (pf_test(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const long long t0 = wait_clock();
     while (!pf_test(bar, parity)) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (wait_clock() - t0 > kWaitLimitCycles) {
             atomicOr(status, kStatusTimeout | site);
             return false;
         }

@@ -358,10 +358,10 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
             };
             auto wait_poll = [&](uint64_t *bar, unsigned par, unsigned site) -> bool {
                 if (mbar_test(bar, par)) return true;
-                const uint64_t t0 = globaltimer_ns();
+                const long long t0 = wait_clock();
                 while (!mbar_test(bar, par)) {
                     try_delta();
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    if (wait_clock() - t0 > kWaitLimitCycles) {
                         atomicOr(a.status, kStatusTimeout | site);
                         return false;
                     }
@@ -415,10 +415,10 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
             }
             if (!ok) *abort_flag = 1;
             if (ok && a.r > 0) {
-                const uint64_t t0 = globaltimer_ns();
+                const long long t0 = wait_clock();
                 while (dn < j) {
                     try_delta();
-                    if (dn < j && globaltimer_ns() - t0 > kWaitLimitNs) {
+                    if (dn < j && wait_clock() - t0 > kWaitLimitCycles) {
                         atomicOr(a.status, kStatusTimeout | kWaitRingFull);
                         break;
                     }

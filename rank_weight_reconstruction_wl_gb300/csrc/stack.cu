@@ -164,7 +164,7 @@ __device__ __forceinline__ float sum1(const StPhase &Q, int n, int slot0, int t,
 {
     const size_t stride = (size_t)Q.nsub * T * kStBox;
     const unsigned long long *p = Q.part + (size_t)slot0 * Q.nsub * T * kStBox + t * kStBox + i;
-    uint64_t t0 = 0;
+    long long t0 = -1;
     for (;;) {
         float s = 0.f;
         bool ok = true;
@@ -175,8 +175,8 @@ __device__ __forceinline__ float sum1(const StPhase &Q, int n, int slot0, int t,
             s += word_val(w);
         }
         if (ok) return s;
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (t0 < 0) t0 = wait_clock();
+        else if (wait_clock() - t0 > kWaitLimitCycles) {
             atomicOr(status, kStatusTimeout | kWaitExchange);
             *ok_out = false;
             return 0.f;
@@ -271,7 +271,7 @@ __device__ __forceinline__ bool sumq(const StPhase &Q, int n, int slot0, int t, 
 {
     const size_t stride = (size_t)Q.nsub * T * kStBox;
     const unsigned long long *base = Q.part + (size_t)slot0 * Q.nsub * T * kStBox + t * kStBox + i0;
-    uint64_t t0 = 0;
+    long long t0 = -1;
     for (;;) {
         float acc[NS][NQ * 4];
 #pragma unroll
@@ -301,8 +301,8 @@ __device__ __forceinline__ bool sumq(const StPhase &Q, int n, int slot0, int t, 
                 for (int e = 0; e < NQ * 4; ++e) out[ps][e] = acc[ps][e];
             return true;
         }
-        if (t0 == 0) t0 = globaltimer_ns();
-        else if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (t0 < 0) t0 = wait_clock();
+        else if (wait_clock() - t0 > kWaitLimitCycles) {
             atomicOr(status, kStatusTimeout | kWaitExchange);
             return false;
         }

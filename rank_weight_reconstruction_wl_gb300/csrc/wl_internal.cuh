@@ -51,9 +51,14 @@ constexpr unsigned kWaitRingFull = 2u;    // consumer waiting for a loaded ring 
 constexpr unsigned kWaitRingEmpty = 4u;   // producer waiting for a free ring stage
 constexpr unsigned kWaitExchange = 8u;    // waiting for cluster peers' partial sums
 
-// Upper bound of every spin-wait in this library.  A wait that runs longer
-// sets kStatusTimeout and returns instead of waiting further.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+// Upper bound of every spin-wait in this library, in SM clock cycles: 4e9
+// cycles is 2 s at 2 GHz (longer at lower clocks).  A wait that runs longer
+// sets kStatusTimeout and returns instead of waiting further.  Waits read the
+// SM's cycle counter, which costs a few cycles; the global nanosecond timer
+// costs far more per read and slowed every polling loop down.
+constexpr long long kWaitLimitCycles = 4000000000ll;
+
+__device__ __forceinline__ long long wait_clock() { return clock64(); }
 
 __device__ __forceinline__ void store_out(void *y, int ydt, int64_t idx, float v)
 {
