@@ -271,9 +271,11 @@ def run_wl(args):
     # ---- dominant kernel, timed per launch with events on its stream ----
     hbm_peak, _, peak_kind = load_peaks()
     if stack.engine == "stack":
-        # the step is nchunk back-to-back launches of the stack kernel, each
-        # over an equal share of the layers
-        nchunk = stack.launches_per_step
+        # the step is the V^T pass (about 7 us) and nchunk back-to-back launches
+        # of the stack kernel, each over an equal share of the layers; the
+        # per-launch time below includes the V^T pass (it understates the
+        # kernel's rate by about 1 %)
+        nchunk = stack.kernel_launches_per_step
         evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                for _ in range(max(3, min(args.steps, 20)))]
         for a0, a1 in evs:
@@ -336,7 +338,7 @@ def run_wl(args):
                        "us_per_token_per_layer": round(ms * 1e3 / (T * nl), 3),
                        "us_per_token_per_stack": round(ms * 1e3 / T, 2),
                        "engine": stack.engine,
-                       "graph": ("one stack-kernel launch per 24 layers" if stack.engine == "stack"
+                       "graph": ("a V^T pass, then one stack-kernel launch per 24 layers" if stack.engine == "stack"
                                  else "CUDA graph replay of the per-projection calls")},
             "roofline": {"bound": "hbm", "kernel": kname,
                          "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",

@@ -61,10 +61,13 @@ class DecoderStack:
         self.graph = None
         self.use_graph = use_graph
         # kernels per layer: fused QKV 1, O 1; the MLP is 2 (gate/up, down) on the
-        # decode path (T <= 8) and 3 (gate/up, GELU, down) on the prefill path
+        # decode path (T <= 8) and on the prefill path where the gate/up kernel
+        # forms h itself (rank padded to 16 at most 32), else 3 (gate/up, GELU,
+        # down)
         lin = (T + 63) // 64 if T <= 64 else 1
-        mlp = 2 if T <= 8 else 3
+        mlp = 2 if (T <= 8 or (r + 15) // 16 * 16 <= 32) else 3
         self.launches_per_step = len(layers) * (2 * lin + mlp)
+        self.kernel_launches_per_step = self.launches_per_step
         self.stk = None
         if engine not in ("auto", "stack", "graph"):
             raise ValueError(f"unknown engine {engine!r}")
@@ -76,7 +79,10 @@ class DecoderStack:
                     raise
         self.engine = "stack" if self.stk is not None else "graph"
         if self.stk is not None:
-            self.launches_per_step = (len(layers) + 23) // 24
+            # one stack-kernel launch per 24 layers, preceded by the V^T pass
+            # (r > 0)
+            self.kernel_launches_per_step = (len(layers) + 23) // 24
+            self.launches_per_step = self.kernel_launches_per_step + (1 if r > 0 else 0)
 
     @property
     def out(self) -> torch.Tensor:
