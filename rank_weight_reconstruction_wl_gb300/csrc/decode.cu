@@ -873,12 +873,12 @@ struct Split {
     int tpc, ngrp, KS, Kc;
 };
 
-static Split plan_split(int ntile, int in, int r_eff, int max_kc, const DeviceInfo *di)
+static Split plan_split(int ntile, int in, int r_eff, int max_kc, const DeviceInfo *di, int tpc_max = 8)
 {
     Split s;
     s.tpc = cdiv(r_eff, 12);
     if (s.tpc < 1) s.tpc = 1;
-    if (s.tpc > 8) s.tpc = 8;
+    if (s.tpc > tpc_max) s.tpc = tpc_max;
     for (;;) {
         s.ngrp = cdiv(ntile, s.tpc);
         int ks = 1;
@@ -922,10 +922,25 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     const int NT = nt_round(cdiv(T, 8));
     int ntile = 0;
     for (int j = 0; j < nproj; ++j) ntile += cdiv(proj[j].out, kBR);
-    // keep x (8*NT rows of K columns) within about 48 KB
+    // keep x (8*NT rows of K columns) within about 48 KB; where the staged x
+    // and the per-tile partial sums still leave no room for two ring stages
+    // (many tokens, long K, large rank), take fewer tiles per row group and
+    // narrower K splits
     int max_kc = (48 * 1024) / (8 * NT * 2);
     max_kc = max_kc < kBK ? kBK : (max_kc / kBK) * kBK;
-    Split sp = plan_split(ntile, (int)in, (int)r, max_kc, di);
+    int tpc_max = 8;
+    Split sp = plan_split(ntile, (int)in, (int)r, max_kc, di, tpc_max);
+    for (;;) {
+        const int xs = x_stride32(sp.Kc);
+        const int need = 8 * NT * xs * 4 + 4 * (sp.tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * (r > 0 ? (int)r : 1) + 512) +
+                         sp.tpc * kBR * 4 + 16;
+        if (ring_stages(need, di) >= 2 || (tpc_max == 1 && max_kc == kBK)) break;
+        if (tpc_max > 1)
+            tpc_max /= 2;
+        else
+            max_kc = max_kc / 2 < kBK ? kBK : (max_kc / 2) / kBK * kBK;
+        sp = plan_split(ntile, (int)in, (int)r, max_kc, di, tpc_max);
+    }
 
     DecArgs a = {};
     a.x = x;

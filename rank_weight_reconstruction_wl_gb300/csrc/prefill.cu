@@ -508,7 +508,10 @@ static std::unordered_map<int, int> g_pf_attr;
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
                          int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st)
 {
-    if (prefill_tiles_applicable(Ktot, r, ydt, false))
+    bool valign = true;
+    for (int j = 0; j < nproj; ++j)
+        if (reinterpret_cast<uintptr_t>(proj[j].V) & 15) valign = false;
+    if (prefill_tiles_applicable(Ktot, r, ydt, false, valign))
         return launch_prefill_tiles(x, proj, nproj, false, y, 0, T, in, Ktot, kmod, r, ydt, 0, 0, st);
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
@@ -648,7 +651,8 @@ wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &
     if (ws_bytes < prefill_mlp_workspace_bytes(T, inter, ydt))
         return fail(WL_ERR_WORKSPACE, "MLP workspace too small for %lld tokens", (long long)T);
     char *w = static_cast<char *>(ws);
-    if (prefill_tiles_applicable(hidden, r, ydt, true)) {
+    const bool gu_valign = ((reinterpret_cast<uintptr_t>(gate.V) | reinterpret_cast<uintptr_t>(up.V)) & 15) == 0;
+    if (prefill_tiles_applicable(hidden, r, ydt, true, gu_valign)) {
         // gate and up in one persistent launch whose epilogue forms h, then down
         const int64_t kmod = (inter + kBKp - 1) / kBKp * kBKp;
         const int64_t ld = ydt == WL_OUT_F32 ? 2 * kmod : kmod;

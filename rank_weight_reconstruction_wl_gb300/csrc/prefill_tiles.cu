@@ -60,6 +60,7 @@ struct TlArgs {
     int T, in, Ktot, kmod, r, rpad, ydt;  // K position k meets W0 column / V row k % kmod
     int BN, bh;        // accumulator columns per tile; W0 rows per box (BN, or BN/2 paired)
     int zc, Kz;        // z columns (rpad per projection of the tile); K of the delta MMA
+    int zlo;           // 1: the delta MMA takes z as bf16 hi + lo parts (fp32 outputs); 0: hi only
     int mtiles, ntiles, ktiles;
     int nst, stage_bytes;
     int vstage;        // 1: V rows of a stage arrive by bulk copy with its tiles
@@ -520,12 +521,13 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
                 const bool nok = n < sg.out;
                 s_tile[e] = nok ? sg.s[n] : 0.f;
                 if (a.r > 0) {
-                    // K positions: [hi part (zc) | lo part (zc) | zero pad]; this
+                    // K positions: [hi part (zc) | lo part (zc, fp32 outputs) | zero pad]; this
                     // row's U (zero past r) sits at slot*rpad within each part
                     const bool vec = (a.r & 7) == 0 && (reinterpret_cast<uintptr_t>(sg.U) & 15) == 0;
                     const bf16 *urow = sg.U + (int64_t)n * a.r;
                     for (int p0 = 0; p0 < a.Kz; p0 += 8) {
-                        const int part = p0 < a.zc ? 0 : (p0 < 2 * a.zc ? 1 : 2);
+                        const int nparts = a.zlo ? 2 : 1;
+                        const int part = p0 < a.zc ? 0 : (p0 < 2 * a.zc && nparts == 2 ? 1 : 2);
                         const int j0 = p0 - part * a.zc - slot * a.rpad;
                         uint4 v = make_uint4(0u, 0u, 0u, 0u);
                         if (part < 2 && j0 >= 0 && j0 < a.r && nok) {
@@ -560,19 +562,21 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
             tc_fence_after();
             if (a.r > 0) {
                 if (nz) {
-                    // z (fp32) -> A_z = [z_hi | z_lo | 0] for this row
+                    // z (fp32) -> A_z = [z_hi | z_lo (fp32 outputs) | 0] for this row
                     const int zh = a.zc / 2;
+                    for (int c0 = half * zh; c0 < (half + 1) * zh; c0 += 32) {
+                    const int nzc = ((half + 1) * zh - c0) >= 32 ? 4 : ((half + 1) * zh - c0) / 8;
                     uint32_t zr[4][8];
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (8 * i < zh) tmem_ld8_nw(tacc + (uint32_t)(a.BN + half * zh + 8 * i), zr[i]);
+                        if (i < nzc) tmem_ld8_nw(tacc + (uint32_t)(a.BN + c0 + 8 * i), zr[i]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        if (8 * i < zh) tmem_wait_ld8(zr[i]);
+                        if (i < nzc) tmem_wait_ld8(zr[i]);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        if (8 * i < zh) {
-                            const int c = half * zh + 8 * i;
+                        if (i < nzc) {
+                            const int c = c0 + 8 * i;
                             uint32_t hi[4], lo[4];
 #pragma unroll
                             for (int p = 0; p < 4; ++p) {
@@ -583,11 +587,13 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
                                 lo[p] = tl_pack(za - ha, zb - hb);
                             }
                             *reinterpret_cast<uint4 *>(az + tl_swz(row, c, kTlBM)) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-                            *reinterpret_cast<uint4 *>(az + tl_swz(row, a.zc + c, kTlBM)) =
-                                make_uint4(lo[0], lo[1], lo[2], lo[3]);
+                            if (a.zlo)
+                                *reinterpret_cast<uint4 *>(az + tl_swz(row, a.zc + c, kTlBM)) =
+                                    make_uint4(lo[0], lo[1], lo[2], lo[3]);
                         }
                     }
-                    for (int c = 2 * a.zc + 8 * half; c < a.Kz; c += 16)
+                    }
+                    for (int c = (a.zlo ? 2 : 1) * a.zc + 8 * half; c < a.Kz; c += 16)
                         *reinterpret_cast<uint4 *>(az + tl_swz(row, c, kTlBM)) = make_uint4(0u, 0u, 0u, 0u);
                 }
                 // acc = s * acc, in place, 32 columns per TMEM round trip
@@ -717,10 +723,15 @@ __global__ void __launch_bounds__(kTlThreads, 1) prefill_tiles_kernel(const __gr
 static std::mutex g_tl_mu;
 static std::unordered_map<int, int> g_tl_attr;
 
-bool prefill_tiles_applicable(int64_t Ktot, int64_t r, int ydt, bool pair)
+bool prefill_tiles_applicable(int64_t Ktot, int64_t r, int ydt, bool pair, bool v_aligned)
 {
     const int64_t rpad = (r + 15) / 16 * 16;
-    if (rpad > (pair ? 32 : 64)) return false;
+    // z of a tile lives in the TMEM buffer next to the accumulator: BN + z
+    // columns = 256.  Paired tiles carry z of two projections: up to rank 32,
+    // or rank 64 with bf16 outputs and V rows loaded by TMA (the V^T writers
+    // hold at most 64 z columns).
+    if (rpad > 64) return false;
+    if (pair && rpad > 32 && !(r == 64 && ydt == WL_OUT_BF16 && v_aligned)) return false;
     // fp32 outputs: the tensor cores' fp32 accumulation error grows with the
     // K chain; long chains go to the split-K kernel
     if (ydt == WL_OUT_F32 && Ktot > 4096) return false;
@@ -737,7 +748,10 @@ wl_status launch_prefill_tiles(const bf16 *x, const wl_proj *proj, int nproj, bo
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
     if (!di) return s;
-    if (!prefill_tiles_applicable(Ktot, r, ydt, pair)) return fail(WL_ERR_UNSUPPORTED, "prefill tiles: shape");
+    bool valign = true;
+    for (int jj = 0; jj < (pair ? 2 : nproj); ++jj)
+        if (reinterpret_cast<uintptr_t>(proj[jj].V) & 15) valign = false;
+    if (!prefill_tiles_applicable(Ktot, r, ydt, pair, valign)) return fail(WL_ERR_UNSUPPORTED, "prefill tiles: shape");
     if (kmod < in || (Ktot > kmod && kmod % 64 != 0)) return fail(WL_ERR_UNSUPPORTED, "prefill tiles: bad K period");
     TlArgs a = {};
     a.nseg = pair ? 2 : nproj;
@@ -750,7 +764,10 @@ wl_status launch_prefill_tiles(const bf16 *x, const wl_proj *proj, int nproj, bo
     a.rpad = r > 0 ? (int)((r + 15) / 16 * 16) : 0;
     a.ydt = ydt;
     a.zc = a.rpad * (pair ? 2 : 1);
-    a.Kz = a.zc > 0 ? (2 * a.zc + 63) / 64 * 64 : 0;
+    // z enters the delta MMA as bf16: the hi part alone moves y by about 2^-9
+    // of the rank-r term (well inside the bf16 bar); fp32 outputs add the lo part
+    a.zlo = ydt == WL_OUT_F32 ? 1 : 0;
+    a.Kz = a.zc > 0 ? ((a.zlo ? 2 : 1) * a.zc + 63) / 64 * 64 : 0;
     a.mtiles = (int)((T + kTlBM - 1) / kTlBM);
     a.ktiles = (int)((Ktot + 63) / 64);
     a.ldy = (int)ldy;

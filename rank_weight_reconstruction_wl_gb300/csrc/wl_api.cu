@@ -88,8 +88,11 @@ static bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_
 static constexpr int64_t kMaxDim = (int64_t)1 << 30;
 
 // Token counts up to this run the HBM-streaming decode kernels; larger ones
-// run the tensor-core prefill kernel.
-static constexpr int64_t kDecodeMaxTokens = 64;
+// run the tensor-core prefill kernels.  Measured on GB300 (fused Q/K/V, graph
+// replay): at 16 tokens the two paths tie on the Gemma-1B shapes (18 vs 19
+// us) and the tensor cores win from there on (32 tokens: 31 vs 19 us; 64:
+// 73 vs 19 us; 5376 -> 4096/2048/2048 at r = 64: 934 vs 66 us at 64 tokens).
+static constexpr int64_t kDecodeMaxTokens = 8;
 // The fused MLP's streaming kernels take up to 8 tokens per pass; more tokens
 // go to the tensor-core path (gate and up in one launch, then down).
 static constexpr int64_t kMlpDecodeMaxTokens = 8;

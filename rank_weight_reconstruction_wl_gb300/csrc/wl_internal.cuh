@@ -113,7 +113,7 @@ size_t prefill_mlp_workspace_bytes(int64_t T, int64_t inter, int ydt);
 // outputs, larger ranks).  pair: proj[0] = gate, proj[1] = up, and y[0] is h
 // (row stride ldy) = gelu_tanh(gate) * up, hw columns per part, the bf16
 // rounding remainder at column hlo (0: none).
-bool prefill_tiles_applicable(int64_t Ktot, int64_t r, int ydt, bool pair);
+bool prefill_tiles_applicable(int64_t Ktot, int64_t r, int ydt, bool pair, bool v_aligned);
 wl_status launch_prefill_tiles(const bf16 *x, const wl_proj *proj, int nproj, bool pair, void *const *y,
                                int64_t ldy, int64_t T, int64_t in, int64_t Ktot, int64_t kmod, int64_t r,
                                int ydt, int64_t hw, int64_t hlo, cudaStream_t st);

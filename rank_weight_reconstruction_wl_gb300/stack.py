@@ -64,7 +64,7 @@ class DecoderStack:
         # decode path (T <= 8) and on the prefill path where the gate/up kernel
         # forms h itself (rank padded to 16 at most 32), else 3 (gate/up, GELU,
         # down)
-        lin = (T + 63) // 64 if T <= 64 else 1
+        lin = 1
         mlp = 2 if (T <= 8 or (r + 15) // 16 * 16 <= 32) else 3
         self.launches_per_step = len(layers) * (2 * lin + mlp)
         self.kernel_launches_per_step = self.launches_per_step

@@ -1,0 +1,52 @@
+"""GPU parity on the large projection set (hidden 5376, intermediate 21504,
+Q/K/V 5376 -> 4096/2048/2048, r = 64) at decode and prefill token counts,
+against the fp64 oracle on sampled tokens (all outputs of those tokens)."""
+import numpy as np
+import pytest
+import torch
+
+import wl_synth
+from tests.parity import assert_parity
+
+pytestmark = pytest.mark.gpu
+
+H, I, Q, KV, R = 5376, 21504, 4096, 2048, 64
+
+
+def _qkv_case(seed, T):
+    g = wl_synth.make_generator(seed)
+    x = wl_synth.draw_x(g, T, H)
+    return x, [wl_synth.draw_theta(g, H, o, R) for o in (Q, KV, KV)]
+
+
+def _tokens(T, n, seed):
+    if T <= n:
+        return np.arange(T)
+    return np.sort(np.random.default_rng(seed).choice(T, n, replace=False))
+
+
+@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (64, torch.float32), (4096, torch.bfloat16)])
+def test_large_qkv(wl, orc, gpu, T, ydt):
+    """T = 1 and 64 run the HBM-streaming kernel (64 tokens with a smaller
+    work split so that it fits in shared memory), T = 4096 the tensor cores."""
+    x, ths = _qkv_case(500 + T, T)
+    ys = wl.wl_qkv_fused(x.to(gpu), *[t.to(gpu) for t in ths], ydt=ydt)
+    torch.cuda.synchronize()
+    assert wl.wl_device_status() == wl.WL_OK, wl.wl_last_error()
+    tok = _tokens(T, 6, T)
+    for y, th, name in zip(ys, ths, "qkv"):
+        ref = orc.linear_sel(x, th, tok=tok)
+        assert_parity(y[torch.as_tensor(tok, device=gpu)], ref, ydt, f"T={T} {name}")
+
+
+@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (64, torch.bfloat16), (4096, torch.bfloat16)])
+def test_large_mlp(wl, orc, gpu, T, ydt):
+    g = wl_synth.make_generator(900 + T)
+    x = wl_synth.draw_x(g, T, H)
+    ths = [wl_synth.draw_theta(g, H, I, R), wl_synth.draw_theta(g, H, I, R), wl_synth.draw_theta(g, I, H, R)]
+    y = wl.wl_mlp_geglu_fused(x.to(gpu), *[t.to(gpu) for t in ths], ydt=ydt)
+    torch.cuda.synchronize()
+    assert wl.wl_device_status() == wl.WL_OK, wl.wl_last_error()
+    tok = _tokens(T, 4, T + 1)
+    ref = orc.mlp_geglu(x, *ths, tok=tok)
+    assert_parity(y[torch.as_tensor(tok, device=gpu)], ref, ydt, f"mlp T={T}")
