@@ -358,6 +358,7 @@ def run_wl(args):
             line["per_call_graph"] = measure_graph_engine(layers, T, r, dev)
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
+            line["large_set"] = measure_large(dev)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = time_oracle_sample(r)
         print(json.dumps(line), flush=True)
@@ -459,6 +460,75 @@ def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
             "layer_gflop": round(flops / 1e9, 2), "parts": out_parts,
             "timing": "CUDA graph replay of the layer's launches (device time)",
             "l2": f"{nlayers} weight sets rotated (larger than L2)"}
+
+
+LARGE = dict(hidden=5376, q=4096, kv=2048, inter=21504, r=64)
+
+
+def measure_large(dev, nsets=2):
+    """The large projection set (hidden 5376, intermediate 21504, Q/K/V
+    5376 -> 4096/2048/2048, r = 64): fused Q/K/V and fused MLP calls at 1, 64
+    and 4096 tokens, rotating over `nsets` weight sets (1.56 GB, larger than
+    L2), timed by CUDA-graph replay.  GB/s of algorithmic bytes at 1 and 64
+    tokens, TFLOP/s at 4096."""
+    import torch
+    import rank_weight_reconstruction_wl_gb300 as wl
+    import wl_synth
+
+    H, Q, KV, I, r = LARGE["hidden"], LARGE["q"], LARGE["kv"], LARGE["inter"], LARGE["r"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(11)
+    sets = [dict(q=wl_synth.draw_theta(g, H, Q, r), k=wl_synth.draw_theta(g, H, KV, r),
+                 v=wl_synth.draw_theta(g, H, KV, r), gate=wl_synth.draw_theta(g, H, I, r),
+                 up=wl_synth.draw_theta(g, H, I, r), down=wl_synth.draw_theta(g, I, H, r))
+            for _ in range(nsets)]
+    st = torch.cuda.Stream(dev)
+
+    def timeit(fn, reps):
+        with torch.cuda.stream(st):
+            for w in sets:
+                fn(w)
+            st.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=st):
+                for _ in range(reps):
+                    for w in sets:
+                        fn(w)
+            gr.replay()
+            st.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(st)
+            gr.replay()
+            a1.record(st)
+            st.synchronize()
+        return a0.elapsed_time(a1) / (reps * nsets) * 1e-3  # s
+
+    out = {"shapes": "hidden 5376, inter 21504, q/k/v 4096/2048/2048, r=64, bf16",
+           "l2": f"{nsets} weight sets rotated (1.56 GB, larger than L2)"}
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    for T in (1, 64, 4096):
+        x = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
+        yq, yk, yv = torch.empty(T, Q, **bf), torch.empty(T, KV, **bf), torch.empty(T, KV, **bf)
+        ym = torch.empty(T, H, **bf)
+        ws = wl.mlp_workspace(T, H, I, r, torch.bfloat16, dev)
+        reps = 10 if T < 4096 else 2
+        tq = timeit(lambda w: wl.wl_qkv_fused(x, w["q"], w["k"], w["v"], outs=(yq, yk, yv), stream=st), reps)
+        tm = timeit(lambda w: wl.wl_mlp_geglu_fused(x, w["gate"], w["up"], w["down"], y=ym, workspace=ws,
+                                                    stream=st), reps)
+        if T < 4096:
+            bq = sum(2 * o * H + 4 * o + 2 * r * (H + o) for o in (Q, KV, KV)) + 2 * T * (H + Q + 2 * KV)
+            bm = (2 * (2 * I * H + 4 * I + 2 * r * (H + I)) + (2 * H * I + 4 * H + 2 * r * (I + H))
+                  + 2 * T * 2 * H)
+            out[f"T{T}"] = {"qkv_us": round(tq * 1e6, 1), "qkv_GBs": round(bq / tq / 1e9, 1),
+                            "mlp_us": round(tm * 1e6, 1), "mlp_GBs": round(bm / tm / 1e9, 1)}
+        else:
+            fq = 2 * T * (H * (Q + 2 * KV) + r * 3 * H + r * (Q + 2 * KV))
+            fm = 2 * T * (3 * H * I + r * 3 * (H + I))
+            out[f"T{T}"] = {"qkv_us": round(tq * 1e6, 1), "qkv_TFLOPs": round(fq / tq / 1e12, 1),
+                            "mlp_us": round(tm * 1e6, 1), "mlp_TFLOPs": round(fm / tm / 1e12, 1)}
+        del ws
+    return out
 
 
 def load_traffic(kernel):
