@@ -356,6 +356,13 @@ def run_wl(args):
             line["clocks"] = ck
         if stack.engine == "stack" and not args.no_compare:
             line["per_call_graph"] = measure_graph_engine(layers, T, r, dev)
+            line["precompute_path"] = measure_precompute(layers, T, r, dev, ms)
+        from rank_weight_reconstruction_wl_gb300.metrics import compression_ratio
+        line["compression"] = {"r": r, "layers": nl,
+                               f"G={nl}": round(compression_ratio(SHAPES, nl, nl, r), 5),
+                               "G=1": round(compression_ratio(SHAPES, nl, 1, r), 5),
+                               "definition": "theta bytes (W0 + s + U + V, all layers and families) / bf16 "
+                                             "dense projection bytes"}
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
             line["large_set"] = measure_large(dev)
@@ -365,6 +372,45 @@ def run_wl(args):
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure_precompute(layers, T, r, dev, ms_weightless, steps=100):
+    """The precompute path ("Serve and generate with weightless", fast path):
+    W_eff of every projection formed once by wl_materialize (bf16), then the
+    same stack run as dense weights (rank 0) on the stack engine."""
+    import torch
+    from rank_weight_reconstruction_wl_gb300.stack import DecoderStack, materialize_layers
+
+    st = torch.cuda.Stream(dev)
+    with torch.cuda.stream(st):
+        materialize_layers(layers[:1])  # warm-up
+        st.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(st)
+        dense = materialize_layers(layers)
+        e1.record(st)
+        st.synchronize()
+    mat_ms = e0.elapsed_time(e1)
+    stk = DecoderStack(dense, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], 0, device=dev, engine="stack")
+    stk.x.normal_()
+    stk.capture()
+    for _ in range(5):
+        stk.step()
+    a0 = torch.cuda.Event(enable_timing=True)
+    a1 = torch.cuda.Event(enable_timing=True)
+    a0.record(stk.stream)
+    for _ in range(steps):
+        stk.step()
+    a1.record(stk.stream)
+    stk.stream.synchronize()
+    ms = a0.elapsed_time(a1) / steps
+    b = layer_bytes(SHAPES, T, 0) * len(layers)
+    return {"value": round(b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "us_per_token_per_layer": round(ms * 1e3 / (T * len(layers)), 3),
+            "step_speed_vs_weightless": round(ms_weightless / ms, 3),
+            "materialize_ms_all_layers": round(mat_ms, 3),
+            "note": "W_eff bf16 of all 182 projections formed once (wl_materialize), then the stack kernel at r=0"}
 
 
 def measure_graph_engine(layers, T, r, dev, steps=30):

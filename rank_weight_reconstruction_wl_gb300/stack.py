@@ -167,3 +167,28 @@ def build_layers(L: int, G: int, T: int, shapes: dict, r: int, seed: int = 0, de
             fams[fam] = th
         layers.append(LayerTheta(**fams))
     return layers
+
+
+def materialize_layers(layers: list[LayerTheta], dt=torch.bfloat16) -> list[LayerTheta]:
+    """The precompute path ("Serve and generate with weightless", fast path):
+    each projection's W_eff = s*W0 + U V^T formed once by wl_materialize, as
+    bundles of rank 0 with s = 1, so that a stack runs them as dense weights."""
+    import wl_synth
+
+    from . import wl_materialize
+
+    out = []
+    for th in layers:
+        fams = {}
+        for fam in ("q", "k", "v", "o", "gate", "up", "down"):
+            t = getattr(th, fam)
+            U = t.U if t.U is not None and t.U.shape[1] > 0 else None
+            V = t.V if U is not None else None
+            W = wl_materialize(t.W0, t.s, U, V, dt=dt)
+            o, i = W.shape
+            fams[fam] = wl_synth.Theta(W, torch.ones(o, dtype=torch.float32, device=W.device),
+                                       torch.zeros(o, 0, dtype=torch.bfloat16, device=W.device),
+                                       torch.zeros(i, 0, dtype=torch.bfloat16, device=W.device))
+        out.append(LayerTheta(**fams))
+    return out
+
