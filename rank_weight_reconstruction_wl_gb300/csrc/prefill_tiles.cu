@@ -8,11 +8,15 @@
 //     acc = x W0^T                       tcgen05.mma kind::f16, fp32 in TMEM
 //     z   = x V      (same K loop)       second MMA into the buffer's z columns
 //     acc = s * acc                      epilogue, TMEM load / multiply / store
-//     acc += [z_hi | z_lo] [U | U]^T     rank-r delta on the tensor cores
+//     acc += z_bf16 U^T                  rank-r delta on the tensor cores (z as
+//                                        bf16 hi + lo parts for fp32 outputs)
 //     y   = cast(acc)                    epilogue
 // z depends only on the token rows and the projection, so a CTA forms it on
-// the first tile of a (rows, projection) run and keeps its bf16 hi + lo split
-// in shared memory for the following tiles of the run.
+// the first tile of a (rows, projection) run and keeps its bf16 split in
+// shared memory for the following tiles of the run.  V is [in, r]: its rows
+// are loaded by TMA as they are and serve as the MN-major B operand of the z
+// MMA (r = 16, 32, 64); for other ranks warps 2-3 write V^T, the K-major
+// operand, into the stage.
 //
 // Paired mode (fused GeGLU MLP, gate and up): a tile holds BN/2 rows of the
 // gate projection and the same BN/2 rows of the up projection, and the
@@ -22,9 +26,8 @@
 //
 // Warp roles (384 threads): warp 0 = TMA producer; warp 1 = TMEM owner and MMA
 // issuer (one thread; it also issues each finished tile's delta MMAs as soon
-// as the epilogue has scaled the accumulator); warps 2-3 = V^T writers (V is
-// [in, r], so the K-major B operand of the z MMA is written by threads); warps
-// 4-11 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31; two warps per
+// as the epilogue has scaled the accumulator); warps 2-3 = V^T writers where
+// V rows are not loaded by TMA; warps 4-11 = epilogue (warp w reads TMEM lanes 32*(w%4) .. +31; two warps per
 // lane quarter split the columns).  Every wait is bounded; a wait that gives
 // up sets the status word and the CTA winds down.
 #include <mutex>

@@ -37,13 +37,6 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
     return v;
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns()
-{
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // Device status bits (OR-ed into the library's status word): kStatusTimeout
 // plus one bit naming the kind of wait that gave up.
 constexpr unsigned kStatusTimeout = 1u;
