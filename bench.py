@@ -129,6 +129,26 @@ class Clocks:
                 "samples": len(sm)}
 
 
+# -------------------------------------------------------- ranks (replicas)
+def max_over_ranks(value: float, device=None) -> float:
+    """The largest of every rank's value (the slowest replica sets the job's
+    time); the value itself without a process group."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units all replicas processed over the
+    slowest replica's time (units per second)."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
 # --------------------------------------------------------------- reference
 def run_reference(args):
     """The fp64 CPU oracle on the host cores, as it stands, on a bounded
@@ -260,12 +280,9 @@ def run_wl(args):
     barrier()
     ck = clocks.stop()
     ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, dev)
     step_bytes = layer_bytes(SHAPES, T, r) * nl
-    value = step_bytes * world / (ms * 1e-3) / 1e9
+    value = job_rate(step_bytes, world, ms) / 1e9
     status = wl.wl_device_status(stack.stream)
 
     # ---- dominant kernel, timed per launch with events on its stream ----
@@ -316,11 +333,8 @@ def run_wl(args):
     t1.record(stack.stream)
     barrier()
     e2e_ms = t0.elapsed_time(t1) / args.steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = step_bytes * world / (e2e_ms * 1e-3) / 1e9
+    e2e_ms = max_over_ranks(e2e_ms, dev)
+    e2e_value = job_rate(step_bytes, world, e2e_ms) / 1e9
 
     if rank == 0:
         line = {
