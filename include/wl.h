@@ -230,6 +230,17 @@ int64_t wl_band_of_layer(int64_t layer, int64_t L, int64_t G);
  */
 wl_status wl_device_status(void *stream);
 
+/*
+ * wl_selftest_wait -- diagnostic for the failure detection above (the pages
+ * have no counterpart): launches on `stream` one kernel that waits, through
+ * the same bounded-wait code as the projection kernels' ring stages, on a
+ * barrier that nothing arrives on.  The wait gives up after its limit (4e9 SM
+ * cycles, about 2 s), so the next wl_device_status(stream) returns
+ * WL_ERR_TIMEOUT; the GPU context stays usable.  Returns WL_OK once launched,
+ * WL_ERR_CUDA if the launch failed.
+ */
+wl_status wl_selftest_wait(void *stream);
+
 /* Message for the last error on the calling thread ("" if none). */
 const char *wl_last_error(void);
 

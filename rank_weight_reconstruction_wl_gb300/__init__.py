@@ -23,7 +23,7 @@ import torch
 __all__ = [
     "WLError", "lib", "library_path", "wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes",
     "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status",
-    "wl_last_error", "wl_version", "WLStack", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
+    "wl_last_error", "wl_version", "wl_selftest_wait", "WLStack", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
     "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
 ]
 
@@ -39,7 +39,7 @@ STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3:
 # Every function include/wl.h declares.
 EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
                     "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_stack_create", "wl_stack_decode",
-                    "wl_stack_destroy", "wl_band_of_layer", "wl_device_status", "wl_last_error", "wl_version")
+                    "wl_stack_destroy", "wl_band_of_layer", "wl_device_status", "wl_last_error", "wl_version", "wl_selftest_wait")
 
 
 class WLError(RuntimeError):
@@ -106,6 +106,8 @@ def lib():
         L.wl_band_of_layer.restype = i64
         L.wl_device_status.argtypes = [vp]
         L.wl_device_status.restype = st
+        L.wl_selftest_wait.argtypes = [vp]
+        L.wl_selftest_wait.restype = st
         L.wl_last_error.restype = C.c_char_p
         L.wl_version.restype = C.c_char_p
         _lib = L
@@ -370,6 +372,14 @@ def wl_device_status(stream=None, device=None) -> int:
     dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
     with torch.cuda.device(dev):
         return int(lib().wl_device_status(_stream(stream, dev)))
+
+
+def wl_selftest_wait(stream=None, device=None):
+    """Launch the diagnostic kernel whose bounded wait gives up (about 2 s);
+    the next wl_device_status() reports WL_ERR_TIMEOUT."""
+    dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+    with torch.cuda.device(dev):
+        _check(lib().wl_selftest_wait(_stream(stream, dev)))
 
 
 def wl_last_error() -> str:

@@ -989,8 +989,15 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     const int per_stage = stage_bytes + 16;
     int nst = (di->max_smem_optin - fixed) / per_stage;
     if (nst > 32) nst = 32;
-    if (nst < 8)
+    if (nst < kWarps)
         return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: these shapes leave room for %d ring stages", nst);
+    // A multiple of the consumer warps: box j of a phase goes to warp j % 8 and
+    // to stage (phase start + j) % nst, so every use of a stage within a phase
+    // falls to one warp, in order.  Otherwise a warp could wait for a stage's
+    // next use before the previous one (another warp's box) has landed, and a
+    // parity wait cannot tell that phase from the one two uses back: it would
+    // return at once, read the stage early and release it out of turn.
+    nst = nst / kWarps * kWarps;
     pl.smem = fixed + nst * per_stage;
 
     // ---- device memory: maps, phases, np/slot0, partial words
