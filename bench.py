@@ -151,9 +151,11 @@ def job_rate(units_per_rank: float, world: int, ms: float) -> float:
 
 # --------------------------------------------------------------- reference
 def run_reference(args):
-    """The fp64 CPU oracle on the host cores, as it stands, on a bounded
-    sample of the same workload (whole layers of the stack at T = 1)."""
+    """The fp64 CPU oracle on the host cores, as it stands, on the same
+    workload: each timed step is one whole pass over the 26-layer stack at
+    T = 1 (every layer's output feeds the next, as on the GPU)."""
     import oracle
+    import torch
     import wl_synth
 
     oracle.build()
@@ -162,43 +164,48 @@ def run_reference(args):
     dims = proj_list(SHAPES)
     g = wl_synth.make_generator(0)
     x = wl_synth.draw_x(g, 1, SHAPES["hidden"])
+    # one layer's theta bundles, reused by every layer of the step: the oracle's
+    # time does not depend on the weights' values, and 26 distinct layers would
+    # cost 26 draws of 54 MB on the host
     thetas = [wl_synth.draw_theta(g, inp, out, r) for inp, out in dims]
 
     def one_layer(xin):
         q = oracle.linear(xin, thetas[0])
         oracle.linear(xin, thetas[1])
         oracle.linear(xin, thetas[2])
-        import torch
-        qb = torch.from_numpy(q).to(torch.bfloat16)
-        o = oracle.linear(qb, thetas[3])
-        ob = torch.from_numpy(o).to(torch.bfloat16)
-        y = oracle.mlp_geglu(ob, thetas[4], thetas[5], thetas[6])
+        o = oracle.linear(torch.from_numpy(q).to(torch.bfloat16), thetas[3])
+        y = oracle.mlp_geglu(torch.from_numpy(o).to(torch.bfloat16), thetas[4], thetas[5], thetas[6])
         return torch.from_numpy(y).to(torch.bfloat16)
 
+    def one_step(xin):
+        for _ in range(L_LAYERS):
+            xin = one_layer(xin)
+        return xin
+
     for _ in range(args.warmup):
-        one_layer(x)
-    times = []
+        one_step(x)
     t_all = time.perf_counter()
     for _ in range(args.steps):
-        t0 = time.perf_counter()
-        one_layer(x)
-        times.append(time.perf_counter() - t0)
+        one_step(x)
     wall = time.perf_counter() - t_all
-    lb = layer_bytes(SHAPES, 1, r)
-    per_layer = sum(times) / len(times)
-    value = lb / per_layer / 1e9
+    per_step = wall / args.steps
+    step_bytes = layer_bytes(SHAPES, 1, r) * L_LAYERS
+    value = step_bytes / per_step / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(per_layer * L_LAYERS * 1e3, 3), "higher_is_better": True,
+        "ms_per_step": round(per_step * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"gemma3-1b decode layer stack, T=1, r={r}, bf16 inputs, "
-                               f"{L_LAYERS} layers (one layer per timed sample)",
+        "config": {"workload": f"gemma3-1b decode layer stack: {L_LAYERS} layers x (fused QKV "
+                               f"1152->1024/256/256, O 1024->1152, fused GeGLU MLP 1152->6912->1152), "
+                               f"T=1, r={r}, bf16 inputs",
+                   "T": 1, "r": r, "layers": L_LAYERS, "step_bytes": step_bytes,
+                   "us_per_token_per_layer": round(per_step * 1e6 / L_LAYERS, 3),
                    "L2": "n/a (CPU)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle",
-                         "sample": f"{args.steps} single layers (1 of {L_LAYERS}) of the stack at T=1; "
-                                   f"ms_per_step extrapolated x{L_LAYERS}; wall {wall:.1f}s"},
+                         "sample": f"{args.steps} whole {L_LAYERS}-layer steps at T=1 after {args.warmup} "
+                                   f"warm-up steps; wall {wall:.1f}s"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -229,8 +236,28 @@ def time_oracle_sample(r, budget_s=12.0):
         if el > budget_s or n >= 5000:
             break
     value = layer_bytes(SHAPES, 1, r) * n / el / 1e9
-    return {"value": round(value, 4), "unit": "GB/s", "cores": oracle.get_threads(),
-            "kind": "oracle", "sample": f"{n} layers of the T=1 stack (of {L_LAYERS}), {el:.1f}s"}
+    cores = oracle.get_threads()
+    # the same layer on one host thread (a short sample)
+    oracle.set_threads(1)
+    try:
+        n1 = 0
+        t1 = time.perf_counter()
+        while True:
+            q = oracle.linear(x, thetas[0])
+            oracle.linear(x, thetas[1])
+            oracle.linear(x, thetas[2])
+            o = oracle.linear(torch.from_numpy(q).to(torch.bfloat16), thetas[3])
+            oracle.mlp_geglu(torch.from_numpy(o).to(torch.bfloat16), *thetas[4:])
+            n1 += 1
+            el1 = time.perf_counter() - t1
+            if el1 > budget_s / 4 or n1 >= 100:
+                break
+    finally:
+        oracle.set_threads(cores)
+    return {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+            "kind": "oracle", "sample": f"{n} layers of the T=1 stack (of {L_LAYERS}), {el:.1f}s",
+            "one_thread": {"value": round(layer_bytes(SHAPES, 1, r) * n1 / el1 / 1e9, 4), "unit": "GB/s",
+                           "cores": 1, "sample": f"{n1} layers, {el1:.1f}s"}}
 
 
 # ---------------------------------------------------------------- wl arm --
@@ -377,8 +404,12 @@ def run_wl(args):
                                "G=1": round(compression_ratio(SHAPES, nl, 1, r), 5),
                                "definition": "theta bytes (W0 + s + U + V, all layers and families) / bf16 "
                                              "dense projection bytes"}
+        if not args.no_grid:
+            line["stack_grid"] = measure_stack_grid(dev)
+            line["materialize"] = measure_materialize(dev)
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
+            line["prefill_T2048_r32"] = measure_prefill(dev, r=32, reps=2)
             line["large_set"] = measure_large(dev)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = time_oracle_sample(r)
@@ -522,6 +553,115 @@ def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
             "l2": f"{nlayers} weight sets rotated (larger than L2)"}
 
 
+def unique_bytes(shapes, L, G, T, r):
+    """Distinct bytes one step touches: G W0 blocks per family, every layer's
+    s, U, V and activations (W0 shared by the layers of a band is counted
+    once)."""
+    b = 0
+    for inp, out in proj_list(shapes):
+        b += G * 2 * out * inp + L * (4 * out + 2 * r * (inp + out) + 2 * T * (inp + out))
+    return b
+
+
+def measure_stack_grid(dev, steps=20, Ts=(1, 32), Gs=(L_LAYERS, 1), ranks=(4, 16, 32)):
+    """The 26-layer stack on the stack engine over T (1: one request; 32: 32
+    requests decoded together), G (26: one W0 per layer, every step streams
+    1.4 GB of distinct weights; 1: one shared W0 set of 53.7 MB, which may stay
+    in L2) and r.  Streamed bytes count every layer's W0 read (the algorithmic
+    bytes of the step); unique bytes count a shared W0 once."""
+    import torch
+    from rank_weight_reconstruction_wl_gb300.stack import DecoderStack, build_layers
+
+    hbm_peak, _, kind = load_peaks()
+    out = {"l2_bytes": torch.cuda.get_device_properties(dev).L2_cache_size, "peak_gbs": hbm_peak,
+           "peak_kind": kind, "timing": f"CUDA events over {steps} steps after 3 warm-up steps"}
+    for T in Ts:
+        for G in Gs:
+            for r in ranks:
+                layers = build_layers(L_LAYERS, G, T, SHAPES, r, seed=17 + r, device=dev)
+                st = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev,
+                                  engine="stack")
+                gx = torch.Generator(device=dev)
+                gx.manual_seed(5)
+                st.x.copy_(torch.randn(T, SHAPES["hidden"], generator=gx, device=dev).to(torch.bfloat16))
+                st.capture()
+                for _ in range(3):
+                    st.step()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st.stream)
+                for _ in range(steps):
+                    st.step()
+                e1.record(st.stream)
+                st.stream.synchronize()
+                ms = e0.elapsed_time(e1) / steps
+                streamed = layer_bytes(SHAPES, T, r) * L_LAYERS
+                uniq = unique_bytes(SHAPES, L_LAYERS, G, T, r)
+                gbs = streamed / (ms * 1e-3) / 1e9
+                out[f"T{T}_G{G}_r{r}"] = {
+                    "ms_per_step": round(ms, 4),
+                    "us_per_token_per_stack": round(ms * 1e3 / T, 3),
+                    "us_per_token_per_layer": round(ms * 1e3 / (T * L_LAYERS), 4),
+                    "streamed_MB": round(streamed / 1e6, 1), "GBs_streamed": round(gbs, 1),
+                    "frac_of_hbm_streamed": round(gbs / hbm_peak, 4),
+                    "unique_MB": round(uniq / 1e6, 1),
+                    "GBs_unique": round(uniq / (ms * 1e-3) / 1e9, 1),
+                    "tflops": round(layer_flops(SHAPES, T, r) * L_LAYERS / (ms * 1e-3) / 1e12, 2)}
+                del st, layers
+                torch.cuda.empty_cache()
+    return out
+
+
+def measure_materialize(dev, r=4, nsets=2, reps=10):
+    """wl_materialize alone: W_eff of the seven Gemma-3-1B projections (one
+    layer) in fp32 and in bf16, output tensors allocated before timing, the
+    launches replayed as a CUDA graph over `nsets` weight sets.  Algorithmic
+    bytes per layer: W0 (2 B/element), s, U and V read once, W_eff written once
+    (4 or 2 B/element)."""
+    import torch
+    import rank_weight_reconstruction_wl_gb300 as wl
+    import wl_synth
+
+    hbm_peak, _, kind = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(13)
+    sets = [[wl_synth.draw_theta(g, inp, o, r) for inp, o in proj_list(SHAPES)] for _ in range(nsets)]
+    st = torch.cuda.Stream(dev)
+    res = {"r": r, "peak_gbs": hbm_peak, "peak_kind": kind,
+           "timing": f"CUDA graph replay, {nsets} weight sets rotated, {reps} passes"}
+    for name, dt, esz in (("f32", torch.float32, 4), ("bf16", torch.bfloat16, 2)):
+        outs = [[torch.empty(o, inp, dtype=dt, device=dev) for inp, o in proj_list(SHAPES)] for _ in range(nsets)]
+
+        def issue():
+            for w, ob in zip(sets, outs):
+                for th, y in zip(w, ob):
+                    wl.wl_materialize(th.W0, th.s, th.U, th.V, dt=dt, out=y, stream=st)
+
+        with torch.cuda.stream(st):
+            issue()
+            st.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr, stream=st):
+                for _ in range(reps):
+                    issue()
+            gr.replay()
+            st.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(st)
+            gr.replay()
+            a1.record(st)
+            st.synchronize()
+        ms = a0.elapsed_time(a1) / (reps * nsets)
+        b = sum(2 * o * inp + 4 * o + 2 * r * (inp + o) + esz * o * inp for inp, o in proj_list(SHAPES))
+        gbs = b / (ms * 1e-3) / 1e9
+        res[name] = {"us_per_layer": round(ms * 1e3, 2), "MB_per_layer": round(b / 1e6, 1),
+                     "GBs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
+                     "launches_per_layer": 7}
+        del outs
+    return res
+
+
 LARGE = dict(hidden=5376, q=4096, kv=2048, inter=21504, r=64)
 
 
@@ -613,6 +753,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true", help="skip the T=2048 prefill measurement")
     ap.add_argument("--no-compare", action="store_true", help="skip timing the per-projection graph engine")
+    ap.add_argument("--no-grid", action="store_true",
+                    help="skip the stack grid (T, G, r) and the wl_materialize measurement")
     ap.add_argument("--engine", default="auto", choices=["auto", "stack", "graph"],
                     help="stack kernel (one launch per 24 layers) or per-projection CUDA graph")
     ap.add_argument("--only-prefill", action="store_true",

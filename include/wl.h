@@ -162,10 +162,10 @@ wl_status wl_materialize(const void *W0, const float *s, const void *U, const vo
  *     g, u    = wl(o; gate), wl(o; up);   h = gelu_tanh(g) * u
  *     x_{l+1} = wl(h; down)
  * Every output is bf16 (round-to-nearest-even of the fp32 result, as for
- * wl_linear with WL_OUT_BF16); h stays fp32 inside the launch, as in
- * wl_mlp_geglu_fused.  Each output of each layer equals, within fp32
- * accumulation order, the single-projection calls on that layer's bf16
- * inputs.  At batch 1 a launch per projection costs more than its weight
+ * wl_linear with WL_OUT_BF16); h keeps fp32 accuracy inside the launch (it
+ * enters the down projection as a bf16 pair hi + lo).  Each output of each
+ * layer equals, within fp32 accumulation order, the single-projection calls
+ * on that layer's bf16 inputs.  At batch 1 a launch per projection costs more than its weight
  * traffic ("What weightless inference costs": at batch-1 decode extra
  * dispatches, not extra arithmetic, dominate), so one launch streams the
  * weights of all L layers and follows the data dependencies inside it.
@@ -191,8 +191,10 @@ typedef struct wl_stack_s *wl_stack;
  * T tokens on the current device.  Allocates the stack's own device tables
  * and scratch (cudaMalloc; freed by wl_stack_destroy) and uploads them
  * synchronously: call it outside stream capture.
- * Limits: 1 <= T <= 4, 0 <= r <= 32; hidden, q.out and gate.out multiples of
- * 64; every layer with the shapes of layer 0; W0 and V 16-byte aligned.
+ * Limits: 1 <= T <= 32, 0 <= r <= 32; hidden, q.out and gate.out multiples
+ * of 64; every layer with the shapes of layer 0; W0 and V 16-byte aligned.
+ * 1..4 tokens and 5..32 tokens run different kernels (the second reduces each
+ * output row tile once and hands it on as bf16).
  * Output buffers of different layers must be distinct and may not alias any
  * input.  Sizes outside these limits give WL_ERR_UNSUPPORTED (use the
  * per-projection calls).  On error *out is NULL.
@@ -204,7 +206,8 @@ wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, const wl_layer_
  * wl_stack_decode -- one pass over all layers of the stack for input x
  * [T, hidden] bf16 (device, 16-byte aligned), asynchronous on `stream`.
  * Writes every output of every layer.  Launches must not overlap: calls on
- * one stream never do.  The launch is cooperative (one CTA per SM); it
+ * one stream never do.  Each step first runs a small kernel that writes V^T
+ * of every projection (and, above 4 tokens, clears the step's flags).  The launch is cooperative (one CTA per SM); it
  * cannot be captured into a CUDA graph on drivers that refuse cooperative
  * launches in capture.
  */

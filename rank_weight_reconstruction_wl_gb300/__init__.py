@@ -304,8 +304,8 @@ class WLStack:
     W0, U, V and fp32 s on one device).  The stack owns one set of bf16 output
     buffers per layer, ``outs[l] = {"yq", "yk", "yv", "yo", "ym"}``;
     ``decode(x)`` writes all of them and returns ``outs[-1]["ym"]``.
-    Raises WLError (WL_ERR_UNSUPPORTED) for sizes the stack kernel does not
-    take (T > 4, r > 32, hidden / q.out / gate.out not multiples of 64).
+    Raises WLError (WL_ERR_UNSUPPORTED) for sizes the stack kernels do not
+    take (T > 32, r > 32, hidden / q.out / gate.out not multiples of 64).
     """
 
     def __init__(self, layers, T: int, device=None):

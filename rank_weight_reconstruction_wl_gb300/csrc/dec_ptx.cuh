@@ -169,6 +169,47 @@ __device__ __forceinline__ const char *prefetch(char *dst, const void *src, int 
     return d;
 }
 
+// Ring wait: a non-blocking test first (the stage is usually loaded long
+// before its consumer reaches it), then the bounded wait.
+__device__ __forceinline__ bool ring_wait(uint64_t *bar, unsigned parity, unsigned *status)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    return mbar_wait(bar, parity, status, kWaitRingFull);
+}
+
+__device__ __forceinline__ bool ring_wait_empty(uint64_t *bar, unsigned parity, unsigned *status)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    return mbar_wait(bar, parity, status, kWaitRingEmpty);
+}
+
+// A 2D tile copy addressed by a shared-memory offset (no address conversion
+// per copy).
+__device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ float gelu_tanh_f32(float v)
 {
     const float c = 0.7978845608028654f;  // sqrt(2/pi)

@@ -221,46 +221,6 @@ __device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&c
     }
 }
 
-// Ring wait: a non-blocking test first (the stage is usually loaded long
-// before its consumer reaches it), then the bounded wait.
-__device__ __forceinline__ bool ring_wait(uint64_t *bar, unsigned parity, unsigned *status)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    return mbar_wait(bar, parity, status, kWaitRingFull);
-}
-
-__device__ __forceinline__ bool ring_wait_empty(uint64_t *bar, unsigned parity, unsigned *status)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    return mbar_wait(bar, parity, status, kWaitRingEmpty);
-}
-
-// Copies addressed by shared-memory offsets (no address conversion per box).
-__device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
-        : "memory");
-}
-
 // Sums of partial words for NQ groups of 4 rows (i0 ..) of token t and NS
 // parts of a row tile of phase Q (n partials from slot0): every load of every
 // slot is issued before the epochs are checked, so a ready input costs one
@@ -745,6 +705,7 @@ using namespace wl;
 
 struct wl_stack_s {
     StackPlan p;
+    WidePlan *wide = nullptr;  // 5..32 tokens: the wide stack kernel (stack_wide.cu)
     std::mutex mu;
 };
 
@@ -768,9 +729,9 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     *out = nullptr;
     if (!layers || !outs || L < 1 || L > 4096)
         return fail(WL_ERR_INVALID_ARG, "wl_stack_create: need 1 <= L <= 4096 layers and outputs");
-    if (T < 1 || T > kStMaxT)
-        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: T = %lld; the stack kernel takes 1..%d tokens", (long long)T,
-                    kStMaxT);
+    if (T < 1 || T > kStackWideMaxT)
+        return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: T = %lld; the stack kernels take 1..%d tokens", (long long)T,
+                    kStackWideMaxT);
     if (r < 0 || r > kStMaxR)
         return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: r = %lld; the stack kernel takes 0..%d", (long long)r,
                     kStMaxR);
@@ -796,6 +757,19 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     wl_status st = WL_OK;
     const DeviceInfo *di = device_info(&st);
     if (!di) return st;
+    if (T > kStMaxT) {
+        WidePlan *wp = nullptr;
+        st = wide_stack_create(&wp, layers, outs, L, T, hidden, r, di);
+        if (st != WL_OK) return st;
+        wl_stack_s *h = new (std::nothrow) wl_stack_s;
+        if (!h) {
+            wide_stack_destroy(wp);
+            return fail(WL_ERR_INVALID_ARG, "wl_stack_create: out of host memory");
+        }
+        h->wide = wp;
+        *out = h;
+        return WL_OK;
+    }
 
     StackPlan pl;
     pl.device = di->device;
@@ -1167,9 +1141,11 @@ extern "C" wl_status wl_stack_decode(wl_stack stk, const void *x, void *stream)
     StackPlan &pl = stk->p;
     int dev = -1;
     cudaGetDevice(&dev);
-    if (dev != pl.device)
-        return fail(WL_ERR_INVALID_ARG, "wl_stack_decode: the stack was built on device %d, current is %d", pl.device,
+    const int built_on = stk->wide ? wide_stack_device(stk->wide) : pl.device;
+    if (dev != built_on)
+        return fail(WL_ERR_INVALID_ARG, "wl_stack_decode: the stack was built on device %d, current is %d", built_on,
                     dev);
+    if (stk->wide) return wide_stack_decode(stk->wide, x, static_cast<cudaStream_t>(stream));
     unsigned epoch;
     {
         std::lock_guard<std::mutex> lk(stk->mu);
@@ -1208,6 +1184,7 @@ extern "C" wl_status wl_stack_decode(wl_stack stk, const void *x, void *stream)
 extern "C" void wl_stack_destroy(wl_stack stk)
 {
     if (!stk) return;
+    if (stk->wide) wide_stack_destroy(stk->wide);
     if (stk->p.dmem) cudaFree(stk->p.dmem);
     delete stk;
 }

@@ -16,9 +16,6 @@ typedef __nv_bfloat16 bf16;
 constexpr int kThreads = 256;  // CTA size of the decode and materialize kernels
 constexpr int kWarps = kThreads / 32;
 
-// Largest token count the CUDA-core decode kernels hold per pass.
-constexpr int kDecodeTT = 8;
-
 // ---------------------------------------------------------------- device --
 // bf16 pair packed in a 32-bit word -> two fp32 values (exact).  The element
 // at the lower address sits in the low half of the word.
@@ -42,7 +39,8 @@ __device__ __forceinline__ uint4 ld_stream16(const void *p)
 constexpr unsigned kStatusTimeout = 1u;
 constexpr unsigned kWaitRingFull = 2u;    // consumer waiting for a loaded ring stage
 constexpr unsigned kWaitRingEmpty = 4u;   // producer waiting for a free ring stage
-constexpr unsigned kWaitExchange = 8u;    // waiting for cluster peers' partial sums
+constexpr unsigned kWaitExchange = 8u;    // waiting for cluster peers' (or other CTAs') partial sums
+constexpr unsigned kWaitDrain = 16u;      // a CTA that gave up could not confirm its copies in flight had landed
 
 // Upper bound of every spin-wait in this library, in SM clock cycles: 4e9
 // cycles is 2 s at 2 GHz (longer at lower clocks).  A wait that runs longer
@@ -113,6 +111,16 @@ wl_status launch_prefill_tiles(const bf16 *x, const wl_proj *proj, int nproj, bo
 wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up, const wl_proj &down,
                              void *y, int64_t T, int64_t hidden, int64_t inter, int64_t r, void *ws,
                              size_t ws_bytes, int ydt, cudaStream_t st);
+// Layer stacks for 5..32 tokens (stack_wide.cu); the caller (wl_stack_create)
+// has validated the layers and sizes.
+struct WidePlan;
+constexpr int kStackWideMaxT = 32;
+wl_status wide_stack_create(WidePlan **out, const wl_layer *layers, const wl_layer_out *outs, int64_t L, int64_t T,
+                            int64_t hidden, int64_t r, const DeviceInfo *di);
+wl_status wide_stack_decode(WidePlan *pl, const void *x, cudaStream_t stream);
+void wide_stack_destroy(WidePlan *pl);
+int wide_stack_device(const WidePlan *pl);
+
 wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U,
                              const bf16 *V, void *W_eff, int64_t out, int64_t in,
                              int64_t r, int dt, cudaStream_t st);

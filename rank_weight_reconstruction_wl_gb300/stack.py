@@ -3,8 +3,8 @@
 Each layer is the projection set of one decoder layer: fused Q/K/V
 (wl_qkv_fused), O (wl_linear) and the fused GeGLU MLP (wl_mlp_geglu_fused).
 Two engines run it:
-  "stack"  one launch per step (per 24 layers) of the library's stack kernel
-           (wl_stack_create / wl_stack_decode), for T <= 4 and r <= 32;
+  "stack"  one launch per step (per 24 layers) of the library's stack kernels
+           (wl_stack_create / wl_stack_decode), for T <= 32 and r <= 32;
   "graph"  the per-projection calls, captured once and replayed as one CUDA
            graph (any T and r).
 The method does not include attention, so the O projection takes the q output
@@ -80,9 +80,10 @@ class DecoderStack:
         self.engine = "stack" if self.stk is not None else "graph"
         if self.stk is not None:
             # one stack-kernel launch per 24 layers, preceded by the V^T pass
-            # (r > 0)
+            # (r > 0; above 4 tokens that pass also clears the step's flags and
+            # always runs)
             self.kernel_launches_per_step = (len(layers) + 23) // 24
-            self.launches_per_step = self.kernel_launches_per_step + (1 if r > 0 else 0)
+            self.launches_per_step = self.kernel_launches_per_step + (1 if (r > 0 or T > 4) else 0)
 
     @property
     def out(self) -> torch.Tensor:

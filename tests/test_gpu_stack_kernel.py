@@ -2,7 +2,9 @@
 output of every layer against the oracle on the bf16 input that projection
 received (parity is per projection: chaining bf16 activations through many
 layers is not part of the contract), repeat launches bit-identical, and the
-limits reported as WL_ERR_UNSUPPORTED."""
+limits reported as WL_ERR_UNSUPPORTED.  1..4 tokens and 5..32 tokens run
+different kernels; both are covered, at ragged small shapes and at the
+Gemma-3-1B layer (32 tokens: the batched-decode case with 32 requests)."""
 import numpy as np
 import pytest
 import torch
@@ -15,10 +17,10 @@ pytestmark = pytest.mark.gpu
 GEMMA = dict(hidden=1152, q=1024, kv=256, inter=6912)
 
 
-def _layers(L, shapes, r, seed, dev, G=None):
+def _layers(L, shapes, r, seed, dev, G=None, kind="random"):
     from rank_weight_reconstruction_wl_gb300.stack import build_layers
 
-    return build_layers(L, G or L, 1, shapes, r, seed=seed, device=dev)
+    return build_layers(L, G or L, 1, shapes, r, seed=seed, device=dev, kind=kind)
 
 
 def _check_layers(orc, layers, stk, x):
@@ -41,6 +43,12 @@ def _check_layers(orc, layers, stk, x):
     (dict(hidden=256, q=128, kv=72, inter=320), 3, 4, 0),
     (dict(hidden=192, q=256, kv=64, inter=640), 2, 2, 32),
     (dict(hidden=64, q=64, kv=16, inter=64), 2, 1, 8),
+    (dict(hidden=128, q=64, kv=40, inter=192), 2, 5, 5),
+    (dict(hidden=256, q=128, kv=72, inter=320), 3, 8, 0),
+    (dict(hidden=128, q=64, kv=64, inter=192), 2, 12, 16),
+    (dict(hidden=192, q=256, kv=64, inter=640), 2, 17, 32),
+    (dict(hidden=128, q=64, kv=24, inter=256), 3, 32, 4),
+    (dict(hidden=64, q=64, kv=16, inter=64), 2, 32, 1),
 ])
 def test_stack_kernel_small(wl, orc, gpu, shapes, L, T, r):
     layers = _layers(L, shapes, r, seed=11 + T + r, dev=gpu)
@@ -54,7 +62,9 @@ def test_stack_kernel_small(wl, orc, gpu, shapes, L, T, r):
     _check_layers(orc, layers, stk, x)
 
 
-@pytest.mark.parametrize("L,G,T,r", [(3, 3, 1, 4), (2, 1, 4, 32), (2, 2, 2, 16)])
+@pytest.mark.parametrize("L,G,T,r", [(3, 3, 1, 4), (2, 1, 4, 32), (2, 2, 2, 16),
+                                     (3, 3, 32, 4), (2, 1, 32, 4), (2, 2, 32, 16), (3, 1, 32, 32),
+                                     (2, 2, 16, 32), (2, 1, 7, 4)])
 def test_stack_kernel_gemma(wl, orc, gpu, L, G, T, r):
     layers = _layers(L, GEMMA, r, seed=21 + r, dev=gpu, G=G)
     stk = wl.WLStack(layers, T, device=gpu)
@@ -67,10 +77,34 @@ def test_stack_kernel_gemma(wl, orc, gpu, L, G, T, r):
     _check_layers(orc, layers, stk, x)
 
 
-def test_stack_kernel_repeat_identical(wl, gpu):
+@pytest.mark.parametrize("T,r", [(1, 4), (4, 32), (32, 4), (32, 32)])
+def test_stack_kernel_delta_dominant(wl, orc, gpu, T, r):
+    """U, V drawn ten times larger than the default, so that the rank-r term
+    (x V) U^T outweighs the W0 term in every projection: the kernels' z = x V
+    and U z paths are then checked well inside the tolerance, not at a few
+    per cent of it."""
+    layers = _layers(2, GEMMA, r, seed=40 + T + r, dev=gpu, kind="delta")
+    cpu = lambda t: t.detach().cpu()
+    th = layers[0].q
+    g = torch.Generator(device=gpu)
+    g.manual_seed(8)
+    x = torch.randn(T, GEMMA["hidden"], generator=g, device=gpu).to(torch.bfloat16)
+    full = orc.linear(cpu(x), wl_synth.Theta(cpu(th.W0), cpu(th.s), cpu(th.U), cpu(th.V)))
+    w0only = orc.linear(cpu(x), wl_synth.Theta(cpu(th.W0), cpu(th.s), 0 * cpu(th.U), 0 * cpu(th.V)))
+    rms = lambda a: float(np.sqrt(np.mean(a ** 2)))
+    assert rms(full - w0only) > 1.5 * rms(w0only)
+    stk = wl.WLStack(layers, T, device=gpu)
+    stk.decode(x)
+    torch.cuda.synchronize()
+    assert wl.wl_device_status() == wl.WL_OK, wl.wl_last_error()
+    _check_layers(orc, layers, stk, x)
+
+
+@pytest.mark.parametrize("T", [1, 32])
+def test_stack_kernel_repeat_identical(wl, gpu, T):
     layers = _layers(4, GEMMA, 4, seed=3, dev=gpu)
-    stk = wl.WLStack(layers, 1, device=gpu)
-    x = torch.randn(1, GEMMA["hidden"], device=gpu).to(torch.bfloat16)
+    stk = wl.WLStack(layers, T, device=gpu)
+    x = torch.randn(T, GEMMA["hidden"], device=gpu).to(torch.bfloat16)
     stk.decode(x)
     first = [{k: v.clone() for k, v in o.items()} for o in stk.outs]
     s = torch.cuda.Stream(gpu)
@@ -83,11 +117,12 @@ def test_stack_kernel_repeat_identical(wl, gpu):
             assert torch.equal(a[k], b[k]), k
 
 
-def test_stack_kernel_matches_per_call_path(wl, gpu):
+@pytest.mark.parametrize("T", [1, 32])
+def test_stack_kernel_matches_per_call_path(wl, gpu, T):
     """The one-launch stack and the per-projection calls on the same inputs."""
     layers = _layers(2, GEMMA, 4, seed=4, dev=gpu)
-    stk = wl.WLStack(layers, 1, device=gpu)
-    x = torch.randn(1, GEMMA["hidden"], device=gpu).to(torch.bfloat16)
+    stk = wl.WLStack(layers, T, device=gpu)
+    x = torch.randn(T, GEMMA["hidden"], device=gpu).to(torch.bfloat16)
     stk.decode(x)
     torch.cuda.synchronize()
     th = layers[0]
@@ -105,7 +140,7 @@ def test_stack_kernel_matches_per_call_path(wl, gpu):
         assert d.max() <= 2e-2 * rms, (b, d.max(), rms)
 
 
-@pytest.mark.parametrize("T,r,hidden", [(5, 4, 128), (1, 33, 128), (1, 4, 96)])
+@pytest.mark.parametrize("T,r,hidden", [(33, 4, 128), (1, 33, 128), (1, 4, 96), (32, 33, 128), (16, 4, 96)])
 def test_stack_kernel_limits(wl, gpu, T, r, hidden):
     shapes = dict(hidden=hidden, q=64, kv=64, inter=128)
     layers = _layers(1, shapes, r, seed=1, dev=gpu)

@@ -18,7 +18,10 @@ with weightless" page: a W0 block, a per-row scale s and a rank-r delta U, V):
 * ``"random"``       the distributions above;
 * ``"degenerate"``   s = 1, U = V = 0 (the map reduces to x W0^T);
 * ``"passthrough"``  same values as degenerate: W0 plays the original weight
-  W ~ N(0, 1/in), so the reconstructed weight equals the original exactly.
+  W ~ N(0, 1/in), so the reconstructed weight equals the original exactly;
+* ``"delta"``        U, V ~ N(0, 0.2^2) (ten times the default): the rank-r
+  term (x V) U^T then outweighs the W0 term, so a test of it is not hidden
+  under the W0 term's share of the tolerance.
 """
 from __future__ import annotations
 
@@ -90,13 +93,14 @@ def draw_x(gen: torch.Generator, T: int, d: int) -> torch.Tensor:
 def draw_theta(gen: torch.Generator, inp: int, out: int, r: int,
                kind: str = "random") -> Theta:
     """Draw W0, s, U, V in that order."""
-    if kind not in ("random", "degenerate", "passthrough"):
+    if kind not in ("random", "degenerate", "passthrough", "delta"):
         raise ValueError(f"unknown kind {kind!r}")
+    uv = 0.2 if kind == "delta" else 0.02
     W0 = (_randn(gen, (out, inp)) * (1.0 / math.sqrt(inp))).to(torch.bfloat16)
     s = 1.0 + 0.1 * _randn(gen, (out,))
-    U = (_randn(gen, (out, r)) * 0.02).to(torch.bfloat16)
-    V = (_randn(gen, (inp, r)) * 0.02).to(torch.bfloat16)
-    if kind != "random":
+    U = (_randn(gen, (out, r)) * uv).to(torch.bfloat16)
+    V = (_randn(gen, (inp, r)) * uv).to(torch.bfloat16)
+    if kind in ("degenerate", "passthrough"):
         s = torch.ones_like(s)
         U = torch.zeros_like(U)
         V = torch.zeros_like(V)
