@@ -111,6 +111,11 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t a[4], uint32_t addr)
                  : "r"(addr));
 }
 
+__device__ __forceinline__ void ldmatrix_x2(uint32_t a[2], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];" : "=r"(a[0]), "=r"(a[1]) : "r"(addr));
+}
+
 // D += A (16x16 bf16, row) * B (16x8 bf16, col), fp32 accumulate.
 __device__ __forceinline__ void mma_16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1)
 {

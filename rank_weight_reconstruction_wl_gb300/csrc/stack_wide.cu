@@ -125,6 +125,7 @@ __device__ __noinline__ void wd_finish(const WdPhase &P, int rt, int np, int slo
     const float *base = P.part + (size_t)slot0 * sstride;
     if (P.kind == kWdGU) {
         const int inter = P.nrt * kWdBox;
+        bf16 *const h = P.h;
         for (int i = threadIdx.x; i < T * 16; i += kThreads) {
             const int t = i >> 4, r4 = (i & 15) * 4;
             float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
@@ -143,7 +144,7 @@ __device__ __noinline__ void wd_finish(const WdPhase &P, int rt, int np, int slo
                 hi[q] = __float2bfloat16_rn(hf[q]);
                 lo[q] = __float2bfloat16_rn(hf[q] - __bfloat162float(hi[q]));
             }
-            bf16 *hp = P.h + (size_t)t * inter + rt * kWdBox + r4;
+            bf16 *hp = h + (size_t)t * inter + rt * kWdBox + r4;
             *reinterpret_cast<uint2 *>(hp) = *reinterpret_cast<uint2 *>(hi);
             *reinterpret_cast<uint2 *>(hp + (size_t)T * inter) = *reinterpret_cast<uint2 *>(lo);
         }
@@ -152,6 +153,8 @@ __device__ __noinline__ void wd_finish(const WdPhase &P, int rt, int np, int slo
         while (si + 1 < P.nseg && rt >= P.seg[si + 1].rt0) ++si;
         const WdSeg &sg = P.seg[si];
         const int row0 = (rt - sg.rt0) * kWdBox;
+        const int out = sg.out;
+        bf16 *const yb = sg.y;
         for (int i = threadIdx.x; i < T * 16; i += kThreads) {
             const int t = i >> 4, r4 = (i & 15) * 4;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -160,15 +163,15 @@ __device__ __noinline__ void wd_finish(const WdPhase &P, int rt, int np, int slo
                 v.x += a.x; v.y += a.y; v.z += a.z; v.w += a.w;
             }
             const float e[4] = {v.x, v.y, v.z, v.w};
-            bf16 *y = sg.y + (size_t)t * sg.out + row0 + r4;
-            if (row0 + r4 + 4 <= sg.out && ((sg.out & 3) == 0)) {
+            bf16 *y = yb + (size_t)t * out + row0 + r4;
+            if (row0 + r4 + 4 <= out && ((out & 3) == 0)) {
                 __align__(8) bf16 hv[4];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) hv[q] = __float2bfloat16_rn(e[q]);
                 *reinterpret_cast<uint2 *>(y) = *reinterpret_cast<uint2 *>(hv);
             } else {
                 for (int q = 0; q < 4; ++q)
-                    if (row0 + r4 + q < sg.out) y[q] = __float2bfloat16_rn(e[q]);
+                    if (row0 + r4 + q < out) y[q] = __float2bfloat16_rn(e[q]);
             }
         }
     }
@@ -187,17 +190,40 @@ __device__ __forceinline__ bool wd_phase(const WdArgs &a, const WdPhase &P, cons
     const int g = lane >> 2, t4 = lane & 3;
     const int lrow = (lane & 7) + ((lane >> 3) & 1) * 8, lchunk = lane >> 4;
     const int mt = warp & 3, tg = warp >> 2;
-    const int T = a.T, r = a.r, zs = a.zstride;
+    // Launch fields in registers: read through the parameter's address they
+    // are generic loads, which the memory clobbers of the barrier operations
+    // would otherwise force to repeat for every box.
+    const int T = a.T, r = a.r, zs = a.zstride, nst = a.nst, sbytes = a.stage_bytes, KB = P.KB;
+    const int us_bytes = a.us_bytes, us_soff = a.us_soff, nsub = P.nsub, kind = P.kind;
+    unsigned *const status = a.status;
+    float *const part = P.part;
     const int Tp = DL ? 2 * T : T;  // staged rows
     const int NT = (Tp + 7) >> 3;
     constexpr int ZPW = DL ? 2 : 1;      // z tiles per warp
     const int nzp = (a.rpad >> 4) * NT;  // z tiles (16 ranks x 8 rows): at most 8 (D: 16)
     const int npc = rec[2], kbs = rec[3];
     const int *pcs = rec + kWdRecHead;
+    // B operands (staged rows = tokens, k contiguous) by ldmatrix: lane l
+    // addresses row l % 8 of matrix l / 8; matrices alternate the k halves
+    // (b0, b1) of consecutive n-tiles.  Rows past the staged ones hold stale
+    // values that only reach output columns the epilogue ignores.
+    const uint32_t xs_lane = smem_u32(xst) + (uint32_t)(((lane & 7) * xs32 + ((lane >> 3) & 1) * 4) * 4);
+    const uint32_t xs_row8 = (uint32_t)(8 * xs32 * 4);  // bytes per n-tile of rows
+    const int bnt = tg * NTW + (lane >> 4);             // n-tile of this lane's x4 address
+    int zm[ZPW], zn[ZPW];
+#pragma unroll
+    for (int z = 0; z < ZPW; ++z) {
+        zm[z] = (warp + 8 * z) / NT;
+        zn[z] = warp + 8 * z - zm[z] * NT;
+    }
+    // ring position of the phase's first box (boxes are consumed in order)
+    int s = qbase % nst;
+    unsigned ph = (unsigned)((qbase / nst) & 1);
+    const uint32_t ring0 = smem_u32(ring);
 
     for (int p = 0; p < npc; ++p) {
         const int *pc = pcs + p * kWdPiece;
-        const int rt = pc[0], sub = pc[1], si = pc[2], row0 = pc[3], j0 = pc[4], nb = pc[5], kb0 = pc[6];
+        const int rt = pc[0], sub = pc[1], si = pc[2], row0 = pc[3], nb = pc[5], kb0 = pc[6];
         const int slot = pc[7], np = pc[8], slot0 = pc[9];
         float acc[NTW][4];
         float zacc[ZPW][4];
@@ -205,69 +231,78 @@ __device__ __forceinline__ bool wd_phase(const WdArgs &a, const WdPhase &P, cons
         for (int n = 0; n < NTW; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
 #pragma unroll
         for (int z = 0; z < ZPW; ++z) zacc[z][0] = zacc[z][1] = zacc[z][2] = zacc[z][3] = 0.f;
-        for (int j = j0; j < j0 + nb; ++j) {
-            const int q = qbase + j;
-            const int s = q % a.nst;
-            const unsigned ph = (unsigned)((q / a.nst) & 1);
+        // staged position of the box's input block: (kb - kbs) mod KB
+        int pos = kb0 - kbs;
+        if (pos < 0) pos += KB;
+        for (int j = 0; j < nb; ++j, pos = (pos + 1 == KB) ? 0 : pos + 1) {
             int w_ok = 1;
-            if (lane == 0) w_ok = !flags[0] && ring_wait(&full[s], ph, a.status);
+            if (lane == 0) w_ok = !flags[0] && ring_wait(&full[s], ph, status);
             w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
             if (!w_ok) {
                 if (lane == 0) flags[0] = 1;
                 break;
             }
-            int pos = kb0 + (j - j0) - kbs;
-            if (pos < 0) pos += P.KB;
-            const uint32_t sb = smem_u32(ring + (size_t)s * a.stage_bytes);
+            const uint32_t sb = ring0 + (uint32_t)(s * sbytes);
+            const uint32_t xb = xs_lane + (uint32_t)(pos * 128);
+            // KS k steps at a time: every fragment load of the group is issued
+            // before its MMAs, so the loads' latency is paid once per group
+            // (two steps where the fragments fit the register budget)
+            constexpr int KS = (NTW >= 4) ? 1 : 2;
 #pragma unroll
-            for (int kin = 0; kin < 4; ++kin) {
-                const int chunk = kin * 2 + lchunk;
-                const int arow = mt * 16 + lrow;
-                uint32_t af[4];
-                ldmatrix_x4(af, sb + arow * 128 + ((chunk ^ (arow & 7)) << 4));
+            for (int k2 = 0; k2 < 4; k2 += KS) {
+                uint32_t af[KS][4], bf[KS][NTW < 2 ? 2 : NTW][2], av[KS][ZPW][4], bz[KS][ZPW][2];
 #pragma unroll
-                for (int n = 0; n < NTW; ++n) {
-                    const int nt = tg * NTW + n;
-                    if (nt < NT) {
-                        uint32_t b0 = 0u, b1 = 0u;
-                        const int tr = nt * 8 + g;
-                        if (tr < Tp) {
-                            const uint32_t *xr = xst + tr * xs32 + pos * 32 + kin * 8 + t4;
-                            b0 = xr[0];
-                            b1 = xr[4];
+                for (int h = 0; h < KS; ++h) {
+                    const int kin = k2 + h;
+                    const int chunk = kin * 2 + lchunk;
+                    const int arow = mt * 16 + lrow;
+                    ldmatrix_x4(af[h], sb + arow * 128 + ((chunk ^ (arow & 7)) << 4));
+#pragma unroll
+                    for (int n = 0; n < NTW; n += 2) {
+                        if (tg * NTW + n < NT) {
+                            if (NTW >= 2) {
+                                uint32_t q4[4];
+                                ldmatrix_x4(q4, xb + (uint32_t)(bnt + n) * xs_row8 + kin * 32);
+                                bf[h][n][0] = q4[0];
+                                bf[h][n][1] = q4[1];
+                                bf[h][n + 1 < NTW ? n + 1 : n][0] = q4[2];
+                                bf[h][n + 1 < NTW ? n + 1 : n][1] = q4[3];
+                            } else {
+                                ldmatrix_x2(bf[h][n], xb + (uint32_t)(tg * NTW) * xs_row8 + kin * 32);
+                            }
                         }
-                        mma_16816(acc[n], af, b0, b1);
+                    }
+#pragma unroll
+                    for (int z = 0; z < ZPW; ++z) {
+                        if (warp + 8 * z < nzp) {
+                            const int zrow = zm[z] * 16 + lrow;
+                            ldmatrix_x4(av[h][z], sb + kWdBoxBytes + zrow * 128 + ((chunk ^ (zrow & 7)) << 4));
+                            ldmatrix_x2(bz[h][z], xb + (uint32_t)zn[z] * xs_row8 + kin * 32);
+                        }
                     }
                 }
 #pragma unroll
-                for (int z = 0; z < ZPW; ++z) {
-                    const int zi = warp + 8 * z;
-                    if (zi < nzp) {
-                        const int zm = zi / NT, zn = zi - zm * NT;
-                        const int zrow = zm * 16 + lrow;
-                        uint32_t av[4];
-                        ldmatrix_x4(av, sb + kWdBoxBytes + zrow * 128 + ((chunk ^ (zrow & 7)) << 4));
-                        uint32_t b0 = 0u, b1 = 0u;
-                        const int tr = zn * 8 + g;
-                        if (tr < Tp) {
-                            const uint32_t *xr = xst + tr * xs32 + pos * 32 + kin * 8 + t4;
-                            b0 = xr[0];
-                            b1 = xr[4];
-                        }
-                        mma_16816(zacc[z], av, b0, b1);
-                    }
+                for (int h = 0; h < KS; ++h) {
+#pragma unroll
+                    for (int n = 0; n < NTW; ++n)
+                        if (tg * NTW + n < NT) mma_16816(acc[n], af[h], bf[h][n][0], bf[h][n][1]);
+#pragma unroll
+                    for (int z = 0; z < ZPW; ++z)
+                        if (warp + 8 * z < nzp) mma_16816(zacc[z], av[h][z], bz[h][z][0], bz[h][z][1]);
                 }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
+            if (++s == nst) {
+                s = 0;
+                ph ^= 1u;
+            }
         }
         // z tiles -> zbuf [staged row][rank]
 #pragma unroll
         for (int z = 0; z < ZPW; ++z) {
-            const int zi = warp + 8 * z;
-            if (zi < nzp) {
-                const int zm = zi / NT, zn = zi - zm * NT;
-                const int col = zn * 8 + 2 * t4, rank = zm * 16 + g;
+            if (warp + 8 * z < nzp) {
+                const int col = zn[z] * 8 + 2 * t4, rank = zm[z] * 16 + g;
                 if (col < Tp) {
                     zbuf[col * zs + rank] = zacc[z][0];
                     zbuf[col * zs + rank + 8] = zacc[z][2];
@@ -283,14 +318,15 @@ __device__ __forceinline__ bool wd_phase(const WdArgs &a, const WdPhase &P, cons
 
         // p = s * acc + U z for this warp's rows and tokens
         const WdSeg &sg = P.seg[si];
-        const char *us = aux_us + (size_t)p * a.us_bytes;
+        const char *us = aux_us + (size_t)p * us_bytes;
         const bf16 *Ur = reinterpret_cast<const bf16 *>(us + (reinterpret_cast<uintptr_t>(sg.U + (size_t)row0 * r) & 15));
-        const float *sr = reinterpret_cast<const float *>(us + a.us_soff + (reinterpret_cast<uintptr_t>(sg.s + row0) & 15));
-        float *dst = P.part + ((size_t)slot * P.nsub + sub) * T * kWdBox;
+        const float *sr = reinterpret_cast<const float *>(us + us_soff + (reinterpret_cast<uintptr_t>(sg.s + row0) & 15));
+        const int sout = sg.out;
+        float *dst = part + ((size_t)slot * nsub + sub) * T * kWdBox;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int row = mt * 16 + g + 8 * hh;
-            const bool rv = row0 + row < sg.out;
+            const bool rv = row0 + row < sout;
             const float sv = rv ? sr[row] : 0.f;
 #pragma unroll
             for (int n = 0; n < NTW; ++n) {
@@ -325,10 +361,10 @@ __device__ __forceinline__ bool wd_phase(const WdArgs &a, const WdPhase &P, cons
         }
         // GU: a CTA holding one part of a pair stores zeros for the other
         const bool next_same = p + 1 < npc && pcs[(p + 1) * kWdPiece] == rt;
-        if (P.kind == kWdGU) {
+        if (kind == kWdGU) {
             const bool has_other = sub == 0 ? next_same : (p > 0 && pcs[(p - 1) * kWdPiece] == rt);
             if (!has_other) {
-                float *o = P.part + ((size_t)slot * P.nsub + (1 - sub)) * T * kWdBox;
+                float *o = part + ((size_t)slot * nsub + (1 - sub)) * T * kWdBox;
                 for (int i = tid; i < T * kWdBox; i += kThreads) o[i] = 0.f;
             }
         }
@@ -364,7 +400,8 @@ __device__ __forceinline__ void wd_fetch_rec(int *recbuf, const int *rec, int re
 }
 
 // NTW / NTWD: n-tiles per warp in the phases other than D / in D (twice the
-// staged rows).
+// staged rows).  Nine warps put three on one SM sub-partition, whose 16K
+// registers then allow at most 168 per thread.
 template <int NTW, int NTWD>
 __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_constant__ WdArgs a)
 {
@@ -398,11 +435,14 @@ __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_
         // ------------------------------------------------------- producer
         if (lane != 0) return;
         const uint32_t w_base = smem_u32(ring);
+        const int nst = a.nst, nph = a.nph, rpad = a.rpad;
+        const unsigned sbytes = (unsigned)a.stage_bytes;
+        unsigned *const status = a.status;
         int s = 0;
         unsigned ph = 0;
         int issued = 0;
         bool ok = true;
-        for (int phi = 0; phi < a.nph && ok; ++phi) {
+        for (int phi = 0; phi < nph && ok; ++phi) {
             const WdPhase &P = a.ph[phi];
             const int nbox = P.nbox, ncta = P.ncta;
             const int b0 = wd_lo(nbox, c, ncta), b1 = wd_lo(nbox, c + 1, ncta);
@@ -431,17 +471,17 @@ __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_
                 }
                 const CUtensorMap *m = si == 2 ? map[2] : si == 1 ? map[1] : map[0];
                 const CUtensorMap *vm = si == 2 ? vtm[2] : si == 1 ? vtm[1] : vtm[0];
-                if (flags[0] || !ring_wait_empty(&empty[s], ph ^ 1u, a.status)) {
+                if (flags[0] || !ring_wait_empty(&empty[s], ph ^ 1u, status)) {
                     ok = false;
                     break;
                 }
                 uint64_t *fb = &full[s];
-                mbar_expect_tx(fb, (unsigned)a.stage_bytes);
-                const uint32_t sdst = w_base + (uint32_t)s * (uint32_t)a.stage_bytes;
+                mbar_expect_tx(fb, sbytes);
+                const uint32_t sdst = w_base + (uint32_t)s * sbytes;
                 tma_load_2d_u32(sdst, m, kb * kWdBox, row0, fb);
-                if (a.rpad) tma_load_2d_u32(sdst + kWdBoxBytes, vm, kb * kWdBox, 0, fb);
+                if (rpad) tma_load_2d_u32(sdst + kWdBoxBytes, vm, kb * kWdBox, 0, fb);
                 ++issued;
-                if (++s == a.nst) {
+                if (++s == nst) {
                     s = 0;
                     ph ^= 1u;
                 }
@@ -455,11 +495,11 @@ __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_
             // let the copies in flight land before the CTA exits; a drain wait
             // that gives up is recorded with its own bit
             flags[2] = 1;
-            const int n = issued < a.nst ? issued : a.nst;
+            const int n = issued < nst ? issued : nst;
             for (int i = 0; i < n; ++i) {
-                s = (s == 0 ? a.nst : s) - 1;
-                if (s == a.nst - 1) ph ^= 1u;
-                if (!mbar_wait(&full[s], ph, a.status, kWaitRingFull)) atomicOr(a.status, kWaitDrain);
+                s = (s == 0 ? nst : s) - 1;
+                if (s == nst - 1) ph ^= 1u;
+                if (!mbar_wait(&full[s], ph, status, kWaitRingFull)) atomicOr(status, kWaitDrain);
             }
         }
         return;
@@ -491,10 +531,12 @@ __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_
             }
             // wait until the producing phase has written the input blocks
             if (P.in_flag) {
+                const unsigned *const in_flag = P.in_flag;
+                const int KB = P.KB;
                 for (int i = tid; i < nk; i += kThreads) {
                     int kb = kbs + i;
-                    if (kb >= P.KB) kb -= P.KB;
-                    if (!wd_poll_flag(P.in_flag + kb, a.status)) {
+                    if (kb >= KB) kb -= KB;
+                    if (!wd_poll_flag(in_flag + kb, a.status)) {
                         flags[0] = 1;
                         break;
                     }
@@ -507,17 +549,19 @@ __global__ void __launch_bounds__(kWdThreads, 1) stack_wide_kernel(const __grid_
             const bool dl = P.kind == kWdD;
             const int rows = dl ? 2 * T : T;
             const int xs32 = 32 * nk + 36;  // 4 mod 32: conflict-free B-operand reads
-            const bf16 *src = P.xin ? P.xin : a.x;
+            const bf16 *const src = P.xin ? P.xin : a.x;
+            const bf16 *const src_lo = P.xin_lo;
+            const int K = P.K, KB = P.KB;
             const int nch = rows * nk * 8;
             for (int i = tid; i < nch; i += kThreads) {
                 const int row = i / (nk * 8);
                 const int rem = i - row * nk * 8;
                 const int pos = rem >> 3, cc = rem & 7;
                 int kb = kbs + pos;
-                if (kb >= P.KB) kb -= P.KB;
+                if (kb >= KB) kb -= KB;
                 const int t = dl ? row >> 1 : row;
-                const bf16 *sp = (dl && (row & 1)) ? P.xin_lo : src;
-                cp_async16(xst + row * xs32 + pos * 32 + cc * 4, sp + (size_t)t * P.K + kb * kWdBox + cc * 8);
+                const bf16 *sp = (dl && (row & 1)) ? src_lo : src;
+                cp_async16(xst + row * xs32 + pos * 32 + cc * 4, sp + (size_t)t * K + kb * kWdBox + cc * 8);
             }
             cp_async_wait_all();
             consumer_sync();
@@ -568,8 +612,15 @@ struct WidePlan {
 
 static int wd_cdiv(int64_t a, int64_t b) { return (int)((a + b - 1) / b); }
 
-// The instantiation for T tokens: n-tiles of 8 rows per warp (two token
-// groups of four warps), D with twice the rows.
+// n-tiles of 8 staged rows per warp (two token groups of four warps) for T
+// tokens; D stages twice the rows.
+static int wide_ntw(int T, bool d)
+{
+    if (d) return T <= 8 ? 1 : (T <= 16 ? 2 : 4);
+    return T <= 16 ? 1 : 2;
+}
+
+// The instantiation for T tokens (template arguments as wide_ntw).
 static const void *wide_kernel(int T)
 {
     if (T <= 8) return (const void *)stack_wide_kernel<1, 1>;
@@ -683,7 +734,8 @@ wl_status wide_stack_create(WidePlan **out, const wl_layer *layers, const wl_lay
             }
             maxp = std::max(maxp, n);
             const int nk = std::min(b1 - b0, P.KB);
-            const int rows = P.kind == kWdD ? 2 * (int)T : (int)T;
+            // every row the B-operand loads can address: two token groups of NTW n-tiles
+            const int rows = 16 * wide_ntw((int)T, P.kind == kWdD);
             xs_max = std::max(xs_max, rows * (32 * nk + 36) * 4);
         }
     }
