@@ -211,16 +211,26 @@ struct Ring {
 
 // Producer (one thread): rows [row0, row0 + 64) x columns [k0, k0 + 64*ktiles)
 // of `map`, two 64x64 boxes per stage.  Rows or columns past the matrix are
-// filled with zeros by the TMA unit.
+// filled with zeros by the TMA unit.  blk: `map` is the k-block view (K a
+// multiple of 64), and one copy fills the stage: a TMA copy costs a fixed few
+// hundred ns, so two 8 KB copies per stage would hold the stream to about 60 %
+// of HBM.  An odd last tile then also loads the next 64 columns, which the
+// consumers skip.
 __device__ __forceinline__ bool produce_tile(Ring &rg, const CUtensorMap *map, int row0, int k0,
-                                             int ktiles, unsigned *status)
+                                             int ktiles, unsigned *status, bool blk)
 {
     for (int kt = 0; kt < ktiles; kt += 2) {
         if (!mbar_wait(&rg.empty[rg.s], rg.ph ^ 1u, status, kWaitRingEmpty)) return false;
-        const int nb = min(2, ktiles - kt);
-        mbar_expect_tx(&rg.full[rg.s], (unsigned)(nb * kBoxBytes));
         char *dst = rg.base + (size_t)rg.s * kStageBytes;
-        for (int b = 0; b < nb; ++b) tma_load_2d(dst + b * kBoxBytes, map, k0 + (kt + b) * kBK, row0, &rg.full[rg.s]);
+        if (blk) {
+            mbar_expect_tx(&rg.full[rg.s], (unsigned)kStageBytes);
+            tma_load_3d(dst, map, 0, row0, k0 / kBK + kt, &rg.full[rg.s]);
+        } else {
+            const int nb = min(2, ktiles - kt);
+            mbar_expect_tx(&rg.full[rg.s], (unsigned)(nb * kBoxBytes));
+            for (int b = 0; b < nb; ++b)
+                tma_load_2d(dst + b * kBoxBytes, map, k0 + (kt + b) * kBK, row0, &rg.full[rg.s]);
+        }
         rg.advance();
     }
     return true;
@@ -245,6 +255,8 @@ __device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_
     // ldmatrix row/chunk of this lane (swizzled 128-byte rows)
     const int lrow = rw * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
     const int lchunk = lane >> 4;
+    // B operands (token rows of x) by shared address
+    const uint32_t xb_ln = smem_u32(xb) + (uint32_t)((g * xs32 + t4) * 4);
     bool ok = true;
     for (int kt = 0; kt < ktiles; kt += 2) {
         int w_ok = 1;
@@ -255,21 +267,31 @@ __device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_
             break;
         }
         const uint32_t sb = smem_u32(rg.base + (size_t)rg.s * kStageBytes);
+        // the stage's fragments first (A of the four k steps of this warp, then
+        // their B words), then the MMAs
+        uint32_t a[4][4], bw[4][NT][2];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
             const int step = kw + 2 * q;    // 0..7 within the stage
             const int box = step >> 2;      // which 64-column box
             const int kin = step & 3;       // 16-column step inside the box
             if (kt + box >= ktiles) continue;
-            uint32_t a[4];
             const int chunk = kin * 2 + lchunk;
-            ldmatrix_x4(a, sb + box * kBoxBytes + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
+            ldmatrix_x4(a[q], sb + box * kBoxBytes + lrow * 128 + ((chunk ^ (lrow & 7)) << 4));
             const int kk = (kt + box) * kBK + kin * 16;  // column relative to k0
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-                const uint32_t *xr = xb + (nt * 8 + g) * xs32 + (kk >> 1) + t4;
-                mma_16816(c[nt], a, xr[0], xr[4]);
+                const uint32_t xa = xb_ln + (uint32_t)((nt * 8 * xs32 + (kk >> 1)) * 4);
+                bw[q][nt][0] = lds_u32(xa);
+                bw[q][nt][1] = lds_u32(xa + 16);
             }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int box = (kw + 2 * q) >> 2;
+            if (kt + box >= ktiles) continue;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_16816(c[nt], a[q], bw[q][nt][0], bw[q][nt][1]);
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&rg.empty[rg.s]);
@@ -404,6 +426,7 @@ struct DecArgs {
     int tpc;     // 64-row tiles per row group
     int nseg, nst, xs32;
     int vbuf, ubuf;  // shared-memory bytes for the prefetched V slice and U rows (0: read in place)
+    int blk;  // 1: the W0 maps are k-block views (one 16 KB copy per ring stage)
     unsigned *status;
 };
 
@@ -445,7 +468,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid
     if (threadIdx.x >= kThreads) {  // ---------------- producer thread
         if (threadIdx.x == kThreads && ktiles > 0)
             for (int tl = 0; tl < ntl; ++tl)
-                if (!produce_tile(c.rg, &sg.map, r0 + tl * kBR, k0, ktiles, a.status)) break;
+                if (!produce_tile(c.rg, &sg.map, r0 + tl * kBR, k0, ktiles, a.status, a.blk)) break;
         return;
     }
 
@@ -523,6 +546,7 @@ struct GateUpArgs {
     float *zd;  // workspace [ngrp*KS][kTokChunk][rp] fp32
     int KS, Kc, tpc, nst, xs32, hmax;
     int vbuf, ubuf, dbuf;  // shared-memory bytes per prefetched V slice / U block / V_down rows (0: in place)
+    int blk;  // 1: the W0 maps are k-block views (one 16 KB copy per ring stage)
     unsigned *status;
 };
 
@@ -569,8 +593,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid
     if (threadIdx.x >= kThreads) {  // ---------------- producer thread
         if (threadIdx.x == kThreads && ktiles > 0)
             for (int tl = 0; tl < ntl; ++tl) {
-                if (!produce_tile(c.rg, &a.mapg, j0 + tl * kBR, k0, ktiles, a.status)) break;
-                if (!produce_tile(c.rg, &a.mapu, j0 + tl * kBR, k0, ktiles, a.status)) break;
+                if (!produce_tile(c.rg, &a.mapg, j0 + tl * kBR, k0, ktiles, a.status, a.blk)) break;
+                if (!produce_tile(c.rg, &a.mapu, j0 + tl * kBR, k0, ktiles, a.status, a.blk)) break;
             }
         return;
     }
@@ -667,6 +691,7 @@ struct DownArgs {
     void *y;
     int KS, Kc, tpc, nst, xs32;
     int ubuf;  // shared-memory bytes for the prefetched U rows (0: read in place)
+    int blk;  // 1: the W0 maps are k-block views (one 16 KB copy per ring stage)
     unsigned *status;
 };
 
@@ -708,7 +733,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
     if (threadIdx.x >= kThreads) {  // ---------------- producer: W_down does not depend on h
         if (threadIdx.x == kThreads && ktiles > 0)
             for (int tl = 0; tl < ntl; ++tl)
-                if (!produce_tile(c.rg, &a.mapd, o0 + tl * kBR, k0, ktiles, a.status)) break;
+                if (!produce_tile(c.rg, &a.mapd, o0 + tl * kBR, k0, ktiles, a.status, a.blk)) break;
         return;
     }
 
@@ -914,6 +939,18 @@ static inline int x_stride32(int width)
     return u16 * 4;
 }
 
+// The W0 map of a projection for the ring: the k-block view (one copy per
+// 16 KB stage) when K is a multiple of 64, else 64 x 64 boxes (two copies).
+static wl_status w0_map(const void *W0, int64_t K, int64_t out, CUtensorMap *m, int *blk)
+{
+    if (K % kBK == 0) {
+        *blk = 1;
+        return tmap_kblocks_bf16(W0, K, out, kBR, 2, m);
+    }
+    *blk = 0;
+    return tmap_2d_bf16(W0, K, out, K, kBK, kBR, m);
+}
+
 static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, void *const *y,
                                  int64_t T, int64_t in, int64_t r, int ydt, cudaStream_t st,
                                  const DeviceInfo *di)
@@ -957,7 +994,7 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     int grp = 0;
     for (int j = 0; j < nproj; ++j) {
         DecSeg &sg = a.seg[j];
-        s = tmap_2d_bf16(proj[j].W0, in, proj[j].out, in, kBK, kBR, &sg.map);
+        s = w0_map(proj[j].W0, in, proj[j].out, &sg.map, &a.blk);
         if (s != WL_OK) return s;
         sg.s = proj[j].s;
         sg.U = static_cast<const bf16 *>(proj[j].U);
@@ -1030,9 +1067,9 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     Split sg = plan_split(cdiv(inter, kBR), hidden, 2 * r, 48 * 1024 / 16, di);
     while (cdiv(inter, kBR * sg.tpc) * sg.KS > kMaxPartials) sg.tpc *= 2;
     sg.ngrp = cdiv(cdiv(inter, kBR), sg.tpc);
-    wl_status s = tmap_2d_bf16(gate.W0, hidden, inter, hidden, kBK, kBR, &g.mapg);
+    wl_status s = w0_map(gate.W0, hidden, inter, &g.mapg, &g.blk);
     if (s != WL_OK) return s;
-    s = tmap_2d_bf16(up.W0, hidden, inter, hidden, kBK, kBR, &g.mapu);
+    s = w0_map(up.W0, hidden, inter, &g.mapu, &g.blk);
     if (s != WL_OK) return s;
     g.x = x;
     g.T = T;
@@ -1079,7 +1116,7 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     DownArgs d = {};
     const int NT = nt_round(cdiv(2 * T, 8));
     Split sd = plan_split(cdiv(hidden, kBR), inter, r, (48 * 1024) / (8 * NT * 2) / kBK * kBK, di);
-    s = tmap_2d_bf16(down.W0, inter, hidden, inter, kBK, kBR, &d.mapd);
+    s = w0_map(down.W0, inter, hidden, &d.mapd, &d.blk);
     if (s != WL_OK) return s;
     d.h = h;
     d.zd = zd;

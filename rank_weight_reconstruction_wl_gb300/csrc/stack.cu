@@ -507,13 +507,26 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             for (int m = 0; m < 4; ++m) cacc[m][0] = cacc[m][1] = cacc[m][2] = cacc[m][3] = 0.f;
 #pragma unroll
             for (int m = 0; m < 2; ++m) zc[m][0] = zc[m][1] = zc[m][2] = zc[m][3] = 0.f;
-            const int rpad = a.rpad;
+            const int rpad = a.rpad, nst = a.nst;
             int cur = -1;  // piece of the accumulators
             int pi = 0;
             float *wbw = wbuf + (size_t)warp * a.wb_floats;
             const size_t wbp = (size_t)kWarps * a.wb_floats;  // stride between pieces
+            // the current piece's first box and k block, and where the next piece starts
+            int pj0 = pcs[0].j0, pkb0 = pcs[0].kb0, nj0 = npc > 1 ? pcs[1].j0 : 0x7fffffff;
+            // ring position of this warp's first box: boxes j = warp, warp + 8, ... and
+            // a ring of a multiple of 8 stages
+            int s = (qbase + warp) % nst;
+            unsigned ph = (unsigned)(((qbase + warp) / nst) & 1);
+            // B operand (token row g of the staged input): by shared address
+            const uint32_t xs_ln = smem_u32(xst) + (uint32_t)((g * a.xs32 + t4) * 4);
             for (int j = warp; j < nbx; j += kWarps) {
-                while (pi + 1 < npc && j >= pcs[pi + 1].j0) ++pi;
+                while (j >= nj0) {
+                    ++pi;
+                    pj0 = nj0;
+                    pkb0 = pcs[pi].kb0;
+                    nj0 = pi + 1 < npc ? pcs[pi + 1].j0 : 0x7fffffff;
+                }
                 if (pi != cur) {
                     if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zc, false, Tp, rpad, lane);
                     for (int p = cur + 1; p < pi; ++p)
@@ -524,9 +537,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     for (int m = 0; m < 2; ++m) zc[m][0] = zc[m][1] = zc[m][2] = zc[m][3] = 0.f;
                     cur = pi;
                 }
-                const int q = qbase + j;
-                const int s = q % a.nst;
-                const unsigned ph = (unsigned)((q / a.nst) & 1);
                 int w_ok = 1;
                 if (lane == 0) w_ok = !flags[0] && ring_wait(&full[s], ph, a.status);
                 w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -534,38 +544,51 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                     if (lane == 0) flags[0] = 1;
                     break;
                 }
-                int pos = pcs[pi].kb0 + (j - pcs[pi].j0) - kbs;
+                int pos = pkb0 + (j - pj0) - kbs;
                 if (pos < 0) pos += KB;
-                const uint32_t sb = smem_u32(ring_w + (size_t)s * sbytes_stage);
+                const uint32_t sb = smem_u32(ring_w) + (uint32_t)(s * sbytes_stage);
+                // the box's B fragments (8 words) first, then per k step the A
+                // fragments of the four row groups and the V^T rows, then the MMAs
+                uint32_t bfr[4][2];
 #pragma unroll
                 for (int kin = 0; kin < 4; ++kin) {
-                    uint32_t b0r = 0u, b1r = 0u;
+                    bfr[kin][0] = bfr[kin][1] = 0u;
                     if (g < Tp) {
-                        const uint32_t *xr = xst + g * a.xs32 + pos * (kStBox / 2) + kin * 8 + t4;
-                        b0r = xr[0];
-                        b1r = xr[4];
+                        const uint32_t xa = xs_ln + (uint32_t)((pos * (kStBox / 2) + kin * 8) * 4);
+                        bfr[kin][0] = lds_u32(xa);
+                        bfr[kin][1] = lds_u32(xa + 16);
                     }
+                }
+#pragma unroll
+                for (int kin = 0; kin < 4; ++kin) {
                     const int chunk = kin * 2 + lchunk;
+                    uint32_t af[4][4], zf[2][4];
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
                         const int row = m * 16 + lrow;
-                        uint32_t af[4];
-                        ldmatrix_x4(af, sb + row * 128 + ((chunk ^ (row & 7)) << 4));
-                        mma_16816(cacc[m], af, b0r, b1r);
+                        ldmatrix_x4(af[m], sb + row * 128 + ((chunk ^ (row & 7)) << 4));
                     }
-                    // z = x V: the V^T rows (ranks) as M, the same token columns
 #pragma unroll
                     for (int m = 0; m < 2; ++m) {
                         if (m * 16 < rpad) {
                             const int row = m * 16 + lrow;
-                            uint32_t af[4];
-                            ldmatrix_x4(af, sb + kStBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
-                            mma_16816(zc[m], af, b0r, b1r);
+                            ldmatrix_x4(zf[m], sb + kStBoxBytes + row * 128 + ((chunk ^ (row & 7)) << 4));
                         }
                     }
+#pragma unroll
+                    for (int m = 0; m < 4; ++m) mma_16816(cacc[m], af[m], bfr[kin][0], bfr[kin][1]);
+                    // z = x V: the V^T rows (ranks) as M, the same token columns
+#pragma unroll
+                    for (int m = 0; m < 2; ++m)
+                        if (m * 16 < rpad) mma_16816(zc[m], zf[m], bfr[kin][0], bfr[kin][1]);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
+                s += kWarps;
+                if (s >= nst) {
+                    s -= nst;
+                    ph ^= 1u;
+                }
             }
             qbase += nbx;
             if (cur >= 0) flush_piece(wbw + cur * wbp, a.wb_zoff, cacc, zc, false, Tp, rpad, lane);
@@ -577,58 +600,60 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             // ---- phase end: p = s * acc + U z per row, the warps' sums added in
             // warp order.  Small r: z over the warps inside the rank loop; larger
             // r: z summed once per (piece, token, rank) first.
-            const bool zfused = r <= 8;
-            if (!zfused) {
+            // the warps' z sums, once per (piece, token, rank); then each row's
+            // acc, its scale and U z.  All reads by shared address.
+            const int wbf = a.wb_floats, wzo = a.wb_zoff;
+            const uint32_t wb_s = smem_u32(wbuf), zs_s = smem_u32(zsum);
+            if (r > 0) {
                 for (int it = tid; it < npc * T * r; it += kThreads) {
                     const int p = it / (T * r), rem = it - p * T * r;
                     const int t = rem / r, j = rem - t * r;
+                    const uint32_t za = wb_s + (uint32_t)(((p * kWarps) * wbf + wzo + t * rpad + j) * 4);
+                    float zw[kWarps], zl[kWarps];
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) {
+                        zw[w] = lds_f32(za + (uint32_t)(w * wbf * 4));
+                        zl[w] = kind == kD ? lds_f32(za + (uint32_t)((w * wbf + T * rpad) * 4)) : 0.f;
+                    }
                     float sum = 0.f;
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) {
-                        const float *wz = wbuf + ((size_t)p * kWarps + w) * a.wb_floats + a.wb_zoff;
-                        sum += wz[t * a.rpad + j];
-                        if (kind == kD) sum += wz[(T + t) * a.rpad + j];
+                        sum += zw[w];
+                        if (kind == kD) sum += zl[w];
                     }
                     zsum[p * kStMaxT * kStMaxR + rem] = sum;
                 }
                 consumer_sync();
             }
+            const int us_soff = (kStBox * r * 2 + 16 + 15) & ~15;
             for (int it = tid; it < npc * T * kStBox; it += kThreads) {
                 const int p = it / (T * kStBox), rem = it - p * T * kStBox;
                 const int t = rem >> 6, row = rem & 63;
                 const Piece pc = pcs[p];
                 const StSeg &sg = P.seg[pc.si];
+                const uint32_t wa = wb_s + (uint32_t)(((p * kWarps) * wbf + t * kStBox + row) * 4);
+                float aw[kWarps], al[kWarps];
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) {
+                    aw[w] = lds_f32(wa + (uint32_t)(w * wbf * 4));
+                    al[w] = kind == kD ? lds_f32(wa + (uint32_t)((w * wbf + T * kStBox) * 4)) : 0.f;
+                }
                 float acc = 0.f, acc_lo = 0.f;
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) {
-                    const float *wb = wbuf + ((size_t)p * kWarps + w) * a.wb_floats;
-                    acc += wb[t * kStBox + row];
-                    if (kind == kD) acc_lo += wb[(T + t) * kStBox + row];
+                    acc += aw[w];
+                    if (kind == kD) acc_lo += al[w];
                 }
                 acc += acc_lo;
                 float v = 0.f;
                 if (pc.row0 + row < sg.out) {
-                    const char *us = aux_us + (size_t)p * a.us_bytes;
-                    const bf16 *Ur = reinterpret_cast<const bf16 *>(
-                        us + (reinterpret_cast<uintptr_t>(sg.U + (size_t)pc.row0 * r) & 15));
-                    const float *sr = reinterpret_cast<const float *>(
-                        us + ((kStBox * r * 2 + 16 + 15) & ~15) + (reinterpret_cast<uintptr_t>(sg.s + pc.row0) & 15));
-                    v = sr[row] * acc;
-                    const float *wz0 = wbuf + (size_t)p * kWarps * a.wb_floats + a.wb_zoff;
-                    const float *zp = zsum + p * kStMaxT * kStMaxR + t * r;
-                    for (int k = 0; k < r; ++k) {
-                        float z = 0.f;
-                        if (zfused) {
-#pragma unroll
-                            for (int w = 0; w < kWarps; ++w) {
-                                z += wz0[(size_t)w * a.wb_floats + t * a.rpad + k];
-                                if (kind == kD) z += wz0[(size_t)w * a.wb_floats + (T + t) * a.rpad + k];
-                            }
-                        } else {
-                            z = zp[k];
-                        }
-                        v = fmaf(__bfloat162float(Ur[row * r + k]), z, v);
-                    }
+                    const uint32_t us = smem_u32(aux_us) + (uint32_t)(p * a.us_bytes);
+                    const uint32_t Ur = us + (uint32_t)(reinterpret_cast<uintptr_t>(sg.U + (size_t)pc.row0 * r) & 15) +
+                                        (uint32_t)(row * r * 2);
+                    const uint32_t sr = us + (uint32_t)us_soff + (uint32_t)(reinterpret_cast<uintptr_t>(sg.s + pc.row0) & 15);
+                    v = lds_f32(sr + (uint32_t)(row * 4)) * acc;
+                    const uint32_t zp = zs_s + (uint32_t)((p * kStMaxT * kStMaxR + t * r) * 4);
+                    for (int k = 0; k < r; ++k) v = fmaf(lds_bf16(Ur + (uint32_t)(k * 2)), lds_f32(zp + (uint32_t)(k * 4)), v);
                 }
                 unsigned long long *sp = P.part + (size_t)pc.slot * P.nsub * T * kStBox;
                 st_word(sp + ((size_t)pc.sub * T + t) * kStBox + row, v, a.epoch);

@@ -80,6 +80,10 @@ wl_status tmap_2d_bf16(const void *base, int64_t inner, int64_t outer, int64_t l
 wl_status tmap_2d_bf16_swz(const void *base, int64_t inner, int64_t outer, int64_t ld_elems,
                            int box_inner, int box_outer, int swizzle_bytes, CUtensorMap *out);
 
+// 3D view of a row-major bf16 matrix [rows, K], K % 64 == 0, whose box is
+// box_rows rows x nblk consecutive 64-column blocks (see tmap.cu).
+wl_status tmap_kblocks_bf16(const void *base, int64_t K, int64_t rows, int box_rows, int nblk, CUtensorMap *out);
+
 // Record a message for wl_last_error() and return the status.
 wl_status fail(wl_status st, const char *fmt, ...);
 wl_status cuda_fail(cudaError_t e, const char *what);
