@@ -889,33 +889,23 @@ static wl_status launch(const void *fn, int grid, int KS, int smem, cudaStream_t
     return WL_OK;
 }
 
-// Work split of `ntile` 64-row tiles with K = in:
+// Work split of `ntile` 64-row tiles with K = in (see plan_balanced):
 //   tpc   tiles per row group: each group forms z = x V once, so more tiles
 //         per group keep the rank-r operand's traffic small next to W0;
-//   KS    K splits (cluster size), chosen to give about one CTA per SM;
+//   KS    K splits (cluster size);
 //   Kc    K elements per split, a multiple of 64 (whole TMA boxes).
 struct Split {
     int tpc, ngrp, KS, Kc;
 };
 
-static Split plan_split(int ntile, int in, int r_eff, int max_kc, const DeviceInfo *di, int tpc_max = 8)
+// Plans are computed once per (launch kind, device, shape) and reused.
+static std::mutex g_plan_mu;
+static std::unordered_map<uint64_t, Split> g_plans;
+static uint64_t plan_key(int kind, int dev, int64_t a, int64_t b, int64_t c, int64_t d)
 {
-    Split s;
-    s.tpc = cdiv(r_eff, 12);
-    if (s.tpc < 1) s.tpc = 1;
-    if (s.tpc > tpc_max) s.tpc = tpc_max;
-    for (;;) {
-        s.ngrp = cdiv(ntile, s.tpc);
-        int ks = 1;
-        while (ks < 8 && (s.ngrp * ks < di->sm_count || round_up(cdiv(in, ks), kBK) > max_kc) &&
-               cdiv(in, 2 * ks) >= kBK)
-            ks *= 2;
-        s.Kc = round_up(cdiv(in, ks), kBK);
-        s.KS = cdiv(in, s.Kc);
-        if (s.ngrp * s.KS * 4 >= di->sm_count * 3 || s.tpc == 1) break;
-        s.tpc = (s.tpc + 1) / 2;
-    }
-    return s;
+    uint64_t h = (uint64_t)kind * 0x9E3779B97F4A7C15ull ^ (uint64_t)dev;
+    for (int64_t v : {a, b, c, d}) h = (h ^ (uint64_t)v) * 0x100000001B3ull + (h >> 29);
+    return h;
 }
 
 // Ring stages that fit next to `other` bytes of shared memory.
@@ -937,6 +927,80 @@ static inline int x_stride32(int width)
     int u16 = width / 8;  // 16-byte units of bf16
     if ((u16 & 1) == 0) u16 += 1;
     return u16 * 4;
+}
+
+// CTAs of `fn` that can be resident at once in clusters of ks with `smem`
+// bytes of shared memory each (cached per device, kernel, ks, smem).
+static int cluster_capacity(const void *fn, int ks, int smem, const DeviceInfo *di)
+{
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    const uint64_t key = ((uint64_t)di->device << 58) ^ ((uint64_t)(uintptr_t)fn << 8) ^ ((uint64_t)smem << 24) ^ (uint64_t)ks;
+    {
+        std::lock_guard<std::mutex> lk(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(ks * di->sm_count));
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)ks;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    int cap;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) == cudaSuccess && n > 0) {
+        cap = n * ks;
+    } else {
+        cudaGetLastError();
+        cap = (di->sm_count / ks) * ks * (smem <= kSmemTarget ? 2 : 1);
+    }
+    std::lock_guard<std::mutex> lk(mu);
+    cache[key] = cap;
+    return cap;
+}
+
+// The split of `ntile` 64-row tiles by `in` columns among CTAs with the least
+// work on the busiest SM.  A row group of tpc tiles and a K split of Kc
+// columns make one CTA; its work is its W0 stream plus its V slice (r_eff
+// ranks) plus a fixed cost per CTA, in units of 64 x 1 tile columns.  CTAs
+// beyond what can be resident at once (cluster placement included), or
+// beyond one per SM, run as further rounds on the same SMs.  smem_of(tpc, Kc)
+// gives the launch's shared memory (< 0: does not fit).
+template <class SmemOf>
+static bool plan_balanced(int ntile, int in, int r_eff, int max_kc, int tpc_max, int max_ctas, const void *fn,
+                          SmemOf smem_of, const DeviceInfo *di, Split *out)
+{
+    double best = 1e30;
+    int best_ctas = 0;
+    bool found = false;
+    for (int tpc = 1; tpc <= tpc_max; ++tpc) {
+        const int ngrp = cdiv(ntile, tpc);
+        for (int ks = 1; ks <= 8; ++ks) {
+            const int Kc = round_up(cdiv(in, ks), kBK);
+            if (Kc > max_kc || cdiv(in, Kc) != ks) continue;
+            const int ctas = ngrp * ks;
+            if (ctas > max_ctas) continue;
+            const int smem = smem_of(tpc, Kc);
+            if (smem < 0) continue;
+            const int cap = cluster_capacity(fn, ks, smem, di);
+            if (cap <= 0) continue;
+            const int usable = cap < di->sm_count ? cap : di->sm_count;
+            const double cost = (double)cdiv(ctas, usable) * ((tpc + r_eff / 64.0) * Kc + 512.0);
+            if (cost < best * 0.999 || (cost < best * 1.001 && ctas < best_ctas)) {
+                best = cost;
+                best_ctas = ctas;
+                *out = Split{tpc, ngrp, ks, Kc};
+                found = true;
+            }
+        }
+    }
+    return found;
 }
 
 // The W0 map of a projection for the ring: the k-block view (one copy per
@@ -965,18 +1029,33 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     // narrower K splits
     int max_kc = (48 * 1024) / (8 * NT * 2);
     max_kc = max_kc < kBK ? kBK : (max_kc / kBK) * kBK;
-    int tpc_max = 8;
-    Split sp = plan_split(ntile, (int)in, (int)r, max_kc, di, tpc_max);
-    for (;;) {
-        const int xs = x_stride32(sp.Kc);
-        const int need = 8 * NT * xs * 4 + 4 * (sp.tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * (r > 0 ? (int)r : 1) + 512) +
-                         sp.tpc * kBR * 4 + 16;
-        if (ring_stages(need, di) >= 2 || (tpc_max == 1 && max_kc == kBK)) break;
-        if (tpc_max > 1)
-            tpc_max /= 2;
-        else
-            max_kc = max_kc / 2 < kBK ? kBK : (max_kc / 2) / kBK * kBK;
-        sp = plan_split(ntile, (int)in, (int)r, max_kc, di, tpc_max);
+    const int rp0 = r > 0 ? (int)r : 1;
+    const dec_fn fn = g_dec[T == 1 ? 0 : 1][nt_index(NT)];
+    // shared memory of a (tpc, Kc) plan, as laid out below
+    auto smem_of = [&](int tpc, int Kc) {
+        const int xs = x_stride32(Kc);
+        int pre = 0;
+        const int vb = round_up(Kc * (int)r * 2 + 16, 16), ub = round_up(tpc * kBR * (int)r * 2 + 16, 16);
+        if (r > 0 && vb + ub <= kPrefetchBudget) pre = vb + ub;
+        const int other = 8 * NT * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp0 + 512) +
+                          tpc * kBR * 4 + 16 + pre;
+        const int nst = ring_stages(other, di);
+        return nst < 2 ? -1 : carve_head_bytes(nst) + other;
+    };
+    s = ensure_attrs((const void *)fn, 0, di);
+    if (s != WL_OK) return s;
+    Split sp;
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        const uint64_t key = plan_key(1, di->device, ntile, in, r, T);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            sp = it->second;
+        } else {
+            if (!plan_balanced(ntile, (int)in, (int)r, max_kc, 8, 1 << 20, (const void *)fn, smem_of, di, &sp))
+                return fail(WL_ERR_UNSUPPORTED, "decode: shapes too large for shared memory");
+            g_plans[key] = sp;
+        }
     }
 
     DecArgs a = {};
@@ -1017,7 +1096,6 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     a.nst = ring_stages(other, di);
     const int smem = carve_head_bytes(a.nst) + other;
     if (a.nst < 2) return fail(WL_ERR_UNSUPPORTED, "decode: shapes too large for shared memory");
-    const dec_fn fn = g_dec[T == 1 ? 0 : 1][nt_index(NT)];
     s = ensure_attrs((const void *)fn, smem, di);
     if (s != WL_OK) return s;
     void *args[] = {&a};
@@ -1064,10 +1142,37 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
 
     // launch 1: gate and up tiles, h, partials of h V_down
     GateUpArgs g = {};
-    Split sg = plan_split(cdiv(inter, kBR), hidden, 2 * r, 48 * 1024 / 16, di);
-    while (cdiv(inter, kBR * sg.tpc) * sg.KS > kMaxPartials) sg.tpc *= 2;
-    sg.ngrp = cdiv(cdiv(inter, kBR), sg.tpc);
-    wl_status s = w0_map(gate.W0, hidden, inter, &g.mapg, &g.blk);
+    const gu_fn gfn = g_gu[T == 1 ? 0 : 1];
+    wl_status s = ensure_attrs((const void *)gfn, 0, di);
+    if (s != WL_OK) return s;
+    // shared memory of a gate/up plan (tpc, Kc), as laid out below
+    auto gsmem_of = [&](int tpc, int Kc) {
+        const int ks = cdiv(hidden, Kc);
+        const int xs = x_stride32(Kc), hmax = cdiv(tpc * kBR, ks) + 1;
+        const int vb = round_up(Kc * r * 2 + 16, 16), ub = round_up(tpc * kBR * r * 2 + 16, 16);
+        const int db = round_up(hmax * r * 2 + 16, 16);
+        const int pre = (r > 0 && 2 * vb + 2 * ub + db <= kPrefetchBudget) ? 2 * vb + 2 * ub + db : 0;
+        const int other = 8 * xs * 4 + 4 * (2 * tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * hmax) +
+                          2 * (tpc * kBR * 4 + 16) + pre;
+        const int nst = ring_stages(other, di);
+        return nst < 2 ? -1 : carve_head_bytes(nst) + other;
+    };
+    Split sg;
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        const uint64_t key = plan_key(2, di->device, inter, hidden, r, T);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            sg = it->second;
+        } else {
+            // gate and up tiles are a pair per CTA: twice the W0 stream and rank work per tile
+            if (!plan_balanced(cdiv(inter, kBR), hidden, 2 * r, 48 * 1024 / 16, 8, kMaxPartials, (const void *)gfn,
+                               gsmem_of, di, &sg))
+                return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
+            g_plans[key] = sg;
+        }
+    }
+    s = w0_map(gate.W0, hidden, inter, &g.mapg, &g.blk);
     if (s != WL_OK) return s;
     s = w0_map(up.W0, hidden, inter, &g.mapu, &g.blk);
     if (s != WL_OK) return s;
@@ -1105,7 +1210,6 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     g.nst = ring_stages(gother, di);
     if (g.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
     const int gsmem = carve_head_bytes(g.nst) + gother;
-    const gu_fn gfn = g_gu[T == 1 ? 0 : 1];
     s = ensure_attrs((const void *)gfn, gsmem, di);
     if (s != WL_OK) return s;
     void *gargs[] = {&g};
@@ -1115,7 +1219,31 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     // launch 2: down tiles, input h as bf16 hi/lo columns
     DownArgs d = {};
     const int NT = nt_round(cdiv(2 * T, 8));
-    Split sd = plan_split(cdiv(hidden, kBR), inter, r, (48 * 1024) / (8 * NT * 2) / kBK * kBK, di);
+    const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
+    s = ensure_attrs((const void *)dfn, 0, di);
+    if (s != WL_OK) return s;
+    auto dsmem_of = [&](int tpc, int Kc) {
+        const int xs = x_stride32(Kc);
+        const int ub = round_up(tpc * kBR * r * 2 + 16, 16);
+        const int pre = (r > 0 && ub <= kPrefetchBudget) ? ub : 0;
+        const int other = 8 * NT * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) + tpc * kBR * 4 + 16 + pre;
+        const int nst = ring_stages(other, di);
+        return nst < 2 ? -1 : carve_head_bytes(nst) + other;
+    };
+    Split sd;
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        const uint64_t key = plan_key(3, di->device, hidden, inter, r, T);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            sd = it->second;
+        } else {
+            if (!plan_balanced(cdiv(hidden, kBR), inter, r, (48 * 1024) / (8 * NT * 2) / kBK * kBK, 8, 1 << 20,
+                               (const void *)dfn, dsmem_of, di, &sd))
+                return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
+            g_plans[key] = sd;
+        }
+    }
     s = w0_map(down.W0, inter, hidden, &d.mapd, &d.blk);
     if (s != WL_OK) return s;
     d.h = h;
@@ -1143,7 +1271,6 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     d.nst = ring_stages(dother, di);
     if (d.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
     const int dsmem = carve_head_bytes(d.nst) + dother;
-    const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
     s = ensure_attrs((const void *)dfn, dsmem, di);
     if (s != WL_OK) return s;
     void *dargs[] = {&d};

@@ -10,10 +10,12 @@
 // not used: their accumulation order is not this one.
 //
 // Tiling: a CTA owns a 64 x 256 tile of W_eff (8 rows x 8 columns per
-// thread).  U and V are staged through shared memory in chunks of 32 ranks
-// (transposed, so each k step reads one float4 pair of V and of U), which
-// keeps the rank-r operands out of HBM after their first read: V is re-read
-// once per 64 output rows, U once per 256 input columns, both from L2.
+// thread).  Each thread loads its W0 chunks before anything else, so that
+// their HBM round trip overlaps the rank-r work.  U and V are staged through
+// shared memory in chunks of 32 ranks (read row-major, coalesced; stored
+// transposed, so each k step reads one float4 pair of V and of U), which keeps
+// the rank-r operands out of HBM after their first read: V is re-read once
+// per 64 output rows, U once per 256 input columns, both from L2.
 #include "wl_internal.cuh"
 
 namespace wl {
@@ -35,6 +37,18 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
     const int i_base = blockIdx.x * kMatCols;
     const int tr = threadIdx.x >> 5;  // rows o_base + tr*8 .. +7
     const int tc = threadIdx.x & 31;  // cols i_base + tc*8 .. +7
+    const int i0 = i_base + tc * 8;
+    const bool col_ok = i0 < in;      // in % 8 == 0: a chunk of 8 columns is all in or all out
+
+    // the thread's W0 chunks first: their HBM round trip overlaps the staging
+    // of U and V and the rank-r products
+    uint4 wv[8];
+#pragma unroll
+    for (int a = 0; a < 8; ++a) {
+        const int o = o_base + tr * 8 + a;
+        wv[a] = (col_ok && o < out) ? *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+    }
 
     float d[8][8];
 #pragma unroll
@@ -44,17 +58,16 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
 
     for (int k0 = 0; k0 < r; k0 += kMatK) {
         const int kn = min(kMatK, r - k0);
-        for (int idx = threadIdx.x; idx < kMatRows * kMatK; idx += kThreads) {
-            const int o = idx / kMatK, k = idx - o * kMatK;
-            float v = 0.f;
-            if (k < kn && o_base + o < out) v = bf2f(U[(int64_t)(o_base + o) * r + k0 + k]);
-            Us[k * kUStr + o] = v;
+        // U rows o_base.., ranks k0..k0+kn-1, and V rows i_base.., the same
+        // ranks, walked in row-major order: consecutive threads read
+        // consecutive ranks of a row, then the next row
+        for (int e = threadIdx.x; e < kMatRows * kn; e += kThreads) {
+            const int o = e / kn, k = e - o * kn;
+            Us[k * kUStr + o] = o_base + o < out ? bf2f(U[(int64_t)(o_base + o) * r + k0 + k]) : 0.f;
         }
-        for (int idx = threadIdx.x; idx < kMatCols * kMatK; idx += kThreads) {
-            const int i = idx / kMatK, k = idx - i * kMatK;
-            float v = 0.f;
-            if (k < kn && i_base + i < in) v = bf2f(V[(int64_t)(i_base + i) * r + k0 + k]);
-            Vs[k * kVStr + i] = v;
+        for (int e = threadIdx.x; e < kMatCols * kn; e += kThreads) {
+            const int i = e / kn, k = e - i * kn;
+            Vs[k * kVStr + i] = i_base + i < in ? bf2f(V[(int64_t)(i_base + i) * r + k0 + k]) : 0.f;
         }
         __syncthreads();
         for (int k = 0; k < kn; ++k) {
@@ -72,16 +85,14 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
         __syncthreads();
     }
 
-    const int i0 = i_base + tc * 8;
-    if (i0 >= in) return;  // in % 8 == 0: a chunk of 8 columns is all in or all out
+    if (!col_ok) return;
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
         const int o = o_base + tr * 8 + a;
         if (o >= out) break;
         const float sv = s[o];
-        const uint4 wv = *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0);
-        const float w0[8] = {bf_lo(wv.x), bf_hi(wv.x), bf_lo(wv.y), bf_hi(wv.y),
-                             bf_lo(wv.z), bf_hi(wv.z), bf_lo(wv.w), bf_hi(wv.w)};
+        const float w0[8] = {bf_lo(wv[a].x), bf_hi(wv[a].x), bf_lo(wv[a].y), bf_hi(wv[a].y),
+                             bf_lo(wv[a].z), bf_hi(wv[a].z), bf_lo(wv[a].w), bf_hi(wv[a].w)};
         float w[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
