@@ -14,6 +14,8 @@ Pinning status (what each function is checked against in ``tests/``):
 
 * ``linear``/``linear_sel``: factored form, brute force, torch float64,
   closed forms, hand-worked golden example -- pinned.
+* ``linear_f32`` (fp32-encoded bundles): brute force, torch float64, equal to
+  ``linear`` on bf16-representable fp32 inputs -- pinned.
 * ``mlp_geglu``: gelu pins + composition from pinned linear pieces -- pinned.
 * ``materialize_f32``/``materialize_bf16``: per-element recomputation with
   Python's correctly rounded float ops and numpy float32, passthrough -- pinned.
@@ -79,6 +81,7 @@ def _configure(L):
                                    vp, i64, _f64p()]
     L.orc_linear_factored.argtypes = [_u16p(), _u16p(), _f32p(), vp, vp, i64, i64, i64,
                                       i64, _f64p()]
+    L.orc_linear_f32w.argtypes = [_f32p(), _f32p(), _f32p(), vp, vp, i64, i64, i64, i64, _f64p()]
     L.orc_gelu_tanh.argtypes = [C.c_double]
     L.orc_gelu_tanh.restype = C.c_double
     L.orc_mlp_geglu.argtypes = ([_u16p()] + [_u16p(), _f32p(), vp, vp] * 3
@@ -235,6 +238,25 @@ def linear_factored(x, theta) -> np.ndarray:
     T = xb.shape[0]
     y = np.empty((T, t.out), np.float64)
     lib().orc_linear_factored(xb, t.W0, t.s, _ptr(t.U), _ptr(t.V), T, t.inp, t.out, t.r, y)
+    return y
+
+
+def linear_f32(x, theta) -> np.ndarray:
+    """y = x W_eff^T in fp64 for an fp32-encoded bundle and fp32 x ("Serve and
+    generate with weightless", "Supported encodings and devices"): every fp32
+    operand converted to fp64 exactly, then the explicit-W_eff form.
+    theta: (W0, s, U, V) fp32 arrays or tensors (U, V may be None when r = 0)."""
+    W0, s_, U, V = (theta if isinstance(theta, (tuple, list)) else (theta.W0, theta.s, theta.U, theta.V))
+    f = lambda a: np.ascontiguousarray(np.asarray(a.cpu() if hasattr(a, "cpu") else a, dtype=np.float32))
+    x = f(x)
+    W0, s_ = f(W0), f(s_)
+    out, inp = W0.shape
+    r = 0 if U is None else int(np.asarray(U.shape)[1])
+    Uc = f(U) if r > 0 else None
+    Vc = f(V) if r > 0 else None
+    T = x.shape[0]
+    y = np.zeros((T, out), dtype=np.float64)
+    lib().orc_linear_f32w(x, W0, s_, _ptr(Uc), _ptr(Vc), T, inp, out, r, y)
     return y
 
 

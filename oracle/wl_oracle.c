@@ -187,6 +187,39 @@ void orc_linear_f64in(const double *x64, const uint16_t *W0, const float *s,
 }
 
 /*
+ * fp32-encoded bundles ("Serve and generate with weightless", "Supported
+ * encodings and devices": the architectures also support float32): x, W0, U,
+ * V and s as fp32, each converted to fp64 exactly; then the same
+ * explicit-W_eff form in fp64:
+ *   W_eff[o,i] = s[o] W0[o,i] + sum_k U[o,k] V[i,k],  y[t,o] = sum_i x[t,i] W_eff[o,i].
+ */
+void orc_linear_f32w(const float *x, const float *W0, const float *s, const float *U,
+                     const float *V, int64_t T, int64_t in, int64_t out, int64_t r,
+                     double *y)
+{
+#pragma omp parallel
+    {
+        double *row = (double *)malloc((size_t)(in > 0 ? in : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t o = 0; o < out; ++o) {
+            for (int64_t i = 0; i < in; ++i) {
+                double w = (double)s[o] * (double)W0[o * in + i];
+                for (int64_t k = 0; k < r; ++k)
+                    w += (double)U[o * r + k] * (double)V[i * r + k];
+                row[i] = w;
+            }
+            for (int64_t t = 0; t < T; ++t) {
+                double acc = 0.0;
+                for (int64_t i = 0; i < in; ++i)
+                    acc += (double)x[t * in + i] * row[i];
+                y[t * out + o] = acc;
+            }
+        }
+        free(row);
+    }
+}
+
+/*
  * Factored form, used only to pin the explicit form against a second,
  * independent evaluation ("In-kernel reconstruction", "The GEMM path"):
  *   y = s[None,:] * (x @ W0.T) + (x @ V) @ U.T

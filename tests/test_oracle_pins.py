@@ -112,6 +112,45 @@ def test_brute_force_tiny(orc, T, n_in, out, r):
     assert np.max(np.abs(y - yb)) <= 1e-13 * scale
 
 
+# ---------------------------------------------- fp32-encoded bundles -------
+# "Serve and generate with weightless", "Supported encodings and devices": the
+# architectures also support float32.  The fp32 entry converts every operand
+# to fp64 exactly; it is pinned like the bf16 one and tied to it.
+@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("n_in,out", [(8, 8), (24, 16)])
+@pytest.mark.parametrize("r", [0, 1, 3])
+def test_f32_brute_force_tiny(orc, T, n_in, out, r):
+    x, th = wl_synth.linear_case_f32(200 + T * 7 + r, T, n_in, out, r)
+    y = orc.linear_f32(x, th)
+    yb = _brute(x, th)
+    scale = np.sqrt(np.mean(yb ** 2)) + 1e-300
+    assert np.max(np.abs(y - yb)) <= 1e-13 * scale
+
+
+def test_f32_degenerate_matches_torch_matmul(orc):
+    x, th = wl_synth.linear_case_f32(1, 4, 1152, 256, 4, kind="degenerate")
+    y = orc.linear_f32(x, th)
+    ref = (x.double() @ th.W0.double().T).numpy()
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.sqrt(np.mean(ref ** 2))
+
+
+def test_f32_matches_gemm_path_float64(orc):
+    """The GEMM-path form s*(x W0^T) + (x V) U^T in torch float64."""
+    x, th = wl_synth.linear_case_f32(2, 5, 320, 96, 7)
+    y = orc.linear_f32(x, th)
+    X, W0, s, U, V = (t.double() for t in (x, th.W0, th.s, th.U, th.V))
+    ref = (s[None, :] * (X @ W0.T) + (X @ V) @ U.T).numpy()
+    assert np.max(np.abs(y - ref)) <= 1e-12 * np.sqrt(np.mean(ref ** 2))
+
+
+def test_f32_equals_bf16_entry_on_bf16_values(orc):
+    """fp32 operands that are bf16 values give exactly the bf16 entry's result
+    (same fp64 values, same order)."""
+    x, th = wl_synth.linear_case(3, 3, 64, 40, 5)
+    th32 = wl_synth.Theta(th.W0.float(), th.s, th.U.float(), th.V.float())
+    assert np.array_equal(orc.linear_f32(x.float(), th32), orc.linear(x, th))
+
+
 # --------------------------------------------- two independent forms -------
 @pytest.mark.parametrize("T,n_in,out,r", [(1, 40, 24, 8), (5, 64, 48, 16), (3, 1152, 64, 4),
                                           (2, 24, 200, 3)])

@@ -36,6 +36,9 @@ __all__ = [
     "draw_x",
     "draw_theta",
     "linear_case",
+    "linear_case_f32",
+    "draw_x_f32",
+    "draw_theta_f32",
     "layer_case",
     "GEMMA_1B",
     "LARGE_SET",
@@ -106,6 +109,37 @@ def draw_theta(gen: torch.Generator, inp: int, out: int, r: int,
         V = torch.zeros_like(V)
     return Theta(W0.contiguous(), s.contiguous(), U.contiguous(), V.contiguous(),
                  {"kind": kind})
+
+
+def draw_x_f32(gen: torch.Generator, T: int, d: int) -> torch.Tensor:
+    """x [T, d] fp32 ~ N(0, 1) (the fp32 encoding of the inputs)."""
+    return _randn(gen, (T, d)).contiguous()
+
+
+def draw_theta_f32(gen: torch.Generator, inp: int, out: int, r: int, kind: str = "random") -> Theta:
+    """An fp32-encoded bundle: the distributions of draw_theta, kept in fp32
+    ("Serve and generate with weightless": the architectures also support
+    float32).  Draw order W0, s, U, V."""
+    if kind not in ("random", "degenerate", "delta"):
+        raise ValueError(f"unknown kind {kind!r}")
+    uv = 0.2 if kind == "delta" else 0.02
+    W0 = _randn(gen, (out, inp)) * (1.0 / math.sqrt(inp))
+    s = 1.0 + 0.1 * _randn(gen, (out,))
+    U = _randn(gen, (out, r)) * uv
+    V = _randn(gen, (inp, r)) * uv
+    if kind == "degenerate":
+        s = torch.ones_like(s)
+        U = torch.zeros_like(U)
+        V = torch.zeros_like(V)
+    return Theta(W0.contiguous(), s.contiguous(), U.contiguous(), V.contiguous(), {"kind": kind, "dtype": "f32"})
+
+
+def linear_case_f32(seed: int, T: int, inp: int, out: int, r: int, kind: str = "random", device="cpu"):
+    """x and one fp32-encoded bundle, drawn in the order x, W0, s, U, V."""
+    g = make_generator(seed, device)
+    x = draw_x_f32(g, T, inp)
+    th = draw_theta_f32(g, inp, out, r, kind)
+    return x, th
 
 
 def linear_case(seed: int, T: int, inp: int, out: int, r: int,
