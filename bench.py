@@ -407,6 +407,7 @@ def run_wl(args):
         if not args.no_grid:
             line["stack_grid"] = measure_stack_grid(dev)
             line["materialize"] = measure_materialize(dev)
+            line["f32_encoding"] = measure_f32(dev)
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
             line["prefill_T2048_r32"] = measure_prefill(dev, r=32, reps=2)
@@ -659,6 +660,63 @@ def measure_materialize(dev, r=4, nsets=2, reps=10):
                      "GBs": round(gbs, 1), "frac": round(gbs / hbm_peak, 4),
                      "launches_per_layer": 7}
         del outs
+    return res
+
+
+# fp32 arithmetic peak of the CUDA cores (the fp32 encoding runs on them):
+# 152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (maximum SM clock)
+F32_ALU_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def measure_f32(dev, r=4, reps=10):
+    """The fp32 encoding ("Serve and generate with weightless", "Supported
+    encodings and devices"): fused Q/K/V of the Gemma-3-1B layer with fp32 x,
+    W0, s, U, V.  T = 1: GB/s of algorithmic bytes (4-byte weights) against
+    HBM; T = 2048: TFLOP/s against the fp32 CUDA-core peak.  CUDA-graph
+    replay over two weight sets (larger than L2 at T = 1 with 4 sets)."""
+    import torch
+    import rank_weight_reconstruction_wl_gb300 as wl
+    import wl_synth
+
+    hbm_peak, _, kind = load_peaks()
+    h, q, kv = SHAPES["hidden"], SHAPES["q"], SHAPES["kv"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(21)
+    sets = [[wl_synth.draw_theta_f32(g, h, o, r) for o in (q, kv, kv)] for _ in range(6)]
+    st = torch.cuda.Stream(dev)
+    res = {"r": r, "peak_gbs": hbm_peak, "peak_kind": kind, "alu_peak_tflops": round(F32_ALU_PEAK_TFLOPS, 1),
+           "alu_peak": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (nominal, maximum clock)"}
+    for T in (1, 2048):
+        x = torch.randn(T, h, generator=g, device=dev)
+        outs = [torch.empty(T, o, dtype=torch.float32, device=dev) for o in (q, kv, kv)]
+        use = sets if T == 1 else sets[:2]
+        with torch.cuda.stream(st):
+            for w in use:
+                wl.wl_qkv_fused(x, *w, outs=outs, ydt=torch.float32, stream=st)
+            st.synchronize()
+            gr = torch.cuda.CUDAGraph()
+            n = reps if T == 1 else 2
+            with torch.cuda.graph(gr, stream=st):
+                for _ in range(n):
+                    for w in use:
+                        wl.wl_qkv_fused(x, *w, outs=outs, ydt=torch.float32, stream=st)
+            gr.replay()
+            st.synchronize()
+            a0 = torch.cuda.Event(enable_timing=True)
+            a1 = torch.cuda.Event(enable_timing=True)
+            a0.record(st)
+            gr.replay()
+            a1.record(st)
+            st.synchronize()
+        sec = a0.elapsed_time(a1) * 1e-3 / (n * len(use))
+        if T == 1:
+            b = sum(4 * o * h + 4 * o + 4 * r * (h + o) for o in (q, kv, kv)) + 4 * T * (h + q + 2 * kv)
+            res["T1"] = {"qkv_us": round(sec * 1e6, 2), "GBs": round(b / sec / 1e9, 1),
+                         "frac_of_hbm": round(b / sec / 1e9 / hbm_peak, 4)}
+        else:
+            f = 2 * T * (h * (q + 2 * kv) + r * 3 * h + r * (q + 2 * kv))
+            res["T2048"] = {"qkv_us": round(sec * 1e6, 1), "TFLOPs": round(f / sec / 1e12, 2),
+                            "frac_of_alu_peak": round(f / sec / 1e12 / F32_ALU_PEAK_TFLOPS, 4)}
     return res
 
 

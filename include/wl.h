@@ -138,6 +138,35 @@ wl_status wl_mlp_geglu_fused_noalloc(const void *x, wl_proj gate, wl_proj up, wl
                                      int64_t r, wl_out_dtype ydt, void *stream);
 
 /*
+ * fp32 encoding ("Serve and generate with weightless", "Supported encodings
+ * and devices": the architectures default to bfloat16 and also support
+ * float32).  The same projection with x, W0, s, U and V all fp32:
+ *     y = s*(x W0^T) + (x V) U^T
+ * computed with fp32 multiply-adds throughout (no bf16 or tf32 rounding of
+ * any operand); y is fp32 or bf16 (ydt).  Layouts as above with 4-byte
+ * elements: x [T,in], W0 [out,in], s [out], U [out,r], V [in,r], y [T,out].
+ * Limits and errors as wl_linear; pointers 16-byte aligned except s, U, V
+ * (4-byte).  Equal, within fp32 accumulation order, to the fp64 product of
+ * the fp32 values.
+ */
+typedef struct {
+    const float *W0;
+    const float *s;
+    const float *U;
+    const float *V;
+    int64_t out;
+} wl_proj_f32;
+
+wl_status wl_linear_f32(const float *x, const float *W0, const float *s, const float *U,
+                        const float *V, void *y, int64_t T, int64_t in, int64_t out,
+                        int64_t r, wl_out_dtype ydt, void *stream);
+
+/* Q, K, V of one fp32 x in one launch (x read once per token tile). */
+wl_status wl_qkv_fused_f32(const float *x, wl_proj_f32 q, wl_proj_f32 k, wl_proj_f32 v,
+                           void *yq, void *yk, void *yv, int64_t T, int64_t in, int64_t r,
+                           wl_out_dtype ydt, void *stream);
+
+/*
  * wl_materialize -- W_eff = s*W0 + U V^T, formed once (the load-time
  * precompute of "Serve and generate with weightless", "Set the fast path on
  * NVIDIA").  W_eff [out, in] of type dt (fp32 or bf16).  Bit-exact with one

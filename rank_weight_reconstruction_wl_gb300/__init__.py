@@ -37,7 +37,7 @@ STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3:
                 4: "WL_ERR_TIMEOUT", 5: "WL_ERR_WORKSPACE"}
 
 # Every function include/wl.h declares.
-EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
+EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_linear_f32", "wl_qkv_fused_f32", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
                     "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_stack_create", "wl_stack_decode",
                     "wl_stack_destroy", "wl_band_of_layer", "wl_device_status", "wl_last_error", "wl_version", "wl_selftest_wait")
 
@@ -49,6 +49,11 @@ class WLError(RuntimeError):
 
 
 class _Proj(C.Structure):
+    _fields_ = [("W0", C.c_void_p), ("s", C.c_void_p), ("U", C.c_void_p), ("V", C.c_void_p),
+                ("out", C.c_int64)]
+
+
+class _ProjF32(C.Structure):
     _fields_ = [("W0", C.c_void_p), ("s", C.c_void_p), ("U", C.c_void_p), ("V", C.c_void_p),
                 ("out", C.c_int64)]
 
@@ -85,6 +90,10 @@ def lib():
         L.wl_linear.restype = st
         L.wl_qkv_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, vp, vp, i64, i64, i64, C.c_int, vp]
         L.wl_qkv_fused.restype = st
+        L.wl_linear_f32.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, C.c_int, vp]
+        L.wl_linear_f32.restype = st
+        L.wl_qkv_fused_f32.argtypes = [vp, _ProjF32, _ProjF32, _ProjF32, vp, vp, vp, i64, i64, i64, C.c_int, vp]
+        L.wl_qkv_fused_f32.restype = st
         L.wl_mlp_workspace_bytes.argtypes = [i64, i64, i64, i64, C.c_int]
         L.wl_mlp_workspace_bytes.restype = C.c_size_t
         L.wl_mlp_geglu_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, i64, i64, i64, i64, vp,
@@ -150,6 +159,18 @@ def _proj(th, inp: int, r: int, name: str):
                  V.data_ptr() if r > 0 else None, out)
 
 
+def _proj_f32(th, inp: int, r: int, name: str):
+    W0, s, U, V = _theta(th)
+    out = W0.shape[0]
+    _need(W0, f"{name}.W0", torch.float32, (out, inp))
+    _need(s, f"{name}.s", torch.float32, (out,))
+    if r > 0:
+        _need(U, f"{name}.U", torch.float32, (out, r))
+        _need(V, f"{name}.V", torch.float32, (inp, r))
+    return _ProjF32(W0.data_ptr(), s.data_ptr(), U.data_ptr() if r > 0 else None,
+                    V.data_ptr() if r > 0 else None, out)
+
+
 def _rank(th) -> int:
     U = _theta(th)[2]
     return 0 if U is None else int(U.shape[1])
@@ -182,11 +203,24 @@ def _check(status: int):
 
 # -------------------------------------------------------------------- API --
 def wl_linear(x, W0, s, U, V, y=None, ydt=torch.bfloat16, stream=None):
-    """y = s*(x W0^T) + (x V) U^T  (x [T,in] bf16 -> y [T,out] bf16/fp32)."""
+    """y = s*(x W0^T) + (x V) U^T  (x [T,in] -> y [T,out] bf16/fp32).
+
+    bf16 x and bundle: wl_linear; fp32 x and bundle (the fp32 encoding):
+    wl_linear_f32."""
     T, inp = x.shape
     out = W0.shape[0]
     r = 0 if U is None else int(U.shape[1])
     code = _ydt(ydt)
+    if x.dtype == torch.float32:
+        p = _proj_f32((W0, s, U, V), inp, r, "theta")
+        if y is None:
+            y = torch.empty(T, out, dtype=_tdt(code), device=x.device)
+        _need(x, "x", torch.float32)
+        _need(y, "y", _tdt(code), (T, out))
+        with torch.cuda.device(x.device):
+            _check(lib().wl_linear_f32(_ptr(x), p.W0, p.s, p.U, p.V, _ptr(y), T, inp, out, r, code,
+                                       _stream(stream, x.device)))
+        return y
     _need(x, "x", torch.bfloat16)
     p = _proj((W0, s, U, V), inp, r, "theta")
     if y is None:
@@ -203,6 +237,17 @@ def wl_qkv_fused(x, q, k, v, outs=None, ydt=torch.bfloat16, stream=None):
     T, inp = x.shape
     r = _rank(q)
     code = _ydt(ydt)
+    if x.dtype == torch.float32:
+        _need(x, "x", torch.float32)
+        ps = [_proj_f32(th, inp, r, n) for th, n in ((q, "q"), (k, "k"), (v, "v"))]
+        if outs is None:
+            outs = tuple(torch.empty(T, p.out, dtype=_tdt(code), device=x.device) for p in ps)
+        for o, p, n in zip(outs, ps, ("yq", "yk", "yv")):
+            _need(o, n, _tdt(code), (T, p.out))
+        with torch.cuda.device(x.device):
+            _check(lib().wl_qkv_fused_f32(_ptr(x), ps[0], ps[1], ps[2], _ptr(outs[0]), _ptr(outs[1]),
+                                          _ptr(outs[2]), T, inp, r, code, _stream(stream, x.device)))
+        return tuple(outs)
     _need(x, "x", torch.bfloat16)
     ps = [_proj(th, inp, r, n) for th, n in ((q, "q"), (k, "k"), (v, "v"))]
     if outs is None:

@@ -184,6 +184,46 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
                                 static_cast<cudaStream_t>(stream));
 }
 
+static wl_status check_theta_f32(const char *name, const float *W0, const float *s, const float *U, const float *V,
+                                 int64_t r)
+{
+    if (!W0 || !s) return fail(WL_ERR_INVALID_ARG, "%s: W0 and s must not be NULL", name);
+    if (r > 0 && (!U || !V)) return fail(WL_ERR_INVALID_ARG, "%s: U and V must not be NULL when r > 0", name);
+    if (!aligned(W0, 16)) return fail(WL_ERR_INVALID_ARG, "%s: W0 must be 16-byte aligned", name);
+    if (!aligned(s, 4) || (r > 0 && (!aligned(U, 4) || !aligned(V, 4))))
+        return fail(WL_ERR_INVALID_ARG, "%s: s, U and V must be 4-byte aligned", name);
+    return WL_OK;
+}
+
+wl_status wl_linear_f32(const float *x, const float *W0, const float *s, const float *U, const float *V,
+                        void *y, int64_t T, int64_t in, int64_t out, int64_t r, wl_out_dtype ydt, void *stream)
+{
+    t_err[0] = '\0';
+    WL_TRY(check_dims(T, in, out, r));
+    WL_TRY(check_io(x, y, ydt));
+    WL_TRY(check_theta_f32("wl_linear_f32", W0, s, U, V, r));
+    WL_TRY(begin());
+    const wl_proj_f32 p = {W0, s, U, V, out};
+    void *ys[1] = {y};
+    return launch_f32_linear(x, &p, 1, ys, T, in, r, ydt, static_cast<cudaStream_t>(stream));
+}
+
+wl_status wl_qkv_fused_f32(const float *x, wl_proj_f32 q, wl_proj_f32 k, wl_proj_f32 v, void *yq, void *yk,
+                           void *yv, int64_t T, int64_t in, int64_t r, wl_out_dtype ydt, void *stream)
+{
+    t_err[0] = '\0';
+    const wl_proj_f32 ps[3] = {q, k, v};
+    void *ys[3] = {yq, yk, yv};
+    const char *names[3] = {"q", "k", "v"};
+    for (int j = 0; j < 3; ++j) {
+        WL_TRY(check_dims(T, in, ps[j].out, r));
+        WL_TRY(check_io(x, ys[j], ydt));
+        WL_TRY(check_theta_f32(names[j], ps[j].W0, ps[j].s, ps[j].U, ps[j].V, r));
+    }
+    WL_TRY(begin());
+    return launch_f32_linear(x, ps, 3, ys, T, in, r, ydt, static_cast<cudaStream_t>(stream));
+}
+
 size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t r, wl_out_dtype ydt)
 {
     if (T < 1 || hidden < 8 || inter < 8 || hidden % 8 || inter % 8 || r < 0 || r > WL_MAX_RANK ||

@@ -125,6 +125,10 @@ wl_status wide_stack_decode(WidePlan *pl, const void *x, cudaStream_t stream);
 void wide_stack_destroy(WidePlan *pl);
 int wide_stack_device(const WidePlan *pl);
 
+// fp32-encoded bundles and inputs (f32_linear.cu)
+wl_status launch_f32_linear(const float *x, const wl_proj_f32 *proj, int nproj, void *const *y, int64_t T,
+                            int64_t in, int64_t r, int ydt, cudaStream_t st);
+
 wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U,
                              const bf16 *V, void *W_eff, int64_t out, int64_t in,
                              int64_t r, int dt, cudaStream_t st);
