@@ -22,6 +22,12 @@ Pinning status (what each function is checked against in ``tests/``):
 * ``f64_to_bf16``/``round_bf16``: exact rational rounding, torch's fp32 cast
   on fp32-representable values -- pinned.
 * ``rel_frobenius``: zero at passthrough, closed form for an added E -- pinned.
+* ``decompose`` (module): W -> theta of a band (mean W0, least-squares s,
+  truncated SVD of the residual for U, V) -- pinned by the passthrough point
+  (exact), an exactly planted rank-r residual, the Eckart-Young error, the
+  normal equations of s and monotonicity in r; planted mistakes fail a pin.
+  The mean / least-squares / SVD steps are a reading for G < L (the pages fix
+  only the passthrough point).
 * ``band_of_layer``: G = L identity, G = 1 constant -- pinned for those G;
   the contiguous-band formula for 1 < G < L is a reading (parity unpinned
   there beyond monotonicity and band sizes).
