@@ -408,6 +408,7 @@ def run_wl(args):
             line["stack_grid"] = measure_stack_grid(dev)
             line["materialize"] = measure_materialize(dev)
             line["f32_encoding"] = measure_f32(dev)
+            line["decompose"] = measure_decompose(dev)
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
             line["prefill_T2048_r32"] = measure_prefill(dev, r=32, reps=2)
@@ -717,6 +718,45 @@ def measure_f32(dev, r=4, reps=10):
             f = 2 * T * (h * (q + 2 * kv) + r * 3 * h + r * (q + 2 * kv))
             res["T2048"] = {"qkv_us": round(sec * 1e6, 1), "TFLOPs": round(f / sec / 1e12, 2),
                             "frac_of_alu_peak": round(f / sec / 1e12 / F32_ALU_PEAK_TFLOPS, 4)}
+    return res
+
+
+def measure_decompose(dev, r=16, p=8, iters=4, n=2):
+    """Dense weights -> theta (wl_decompose_band) for one band of n layers of
+    each Gemma-3-1B projection shape.  Algorithmic bytes per layer: one pass
+    over W and W0 for s and 2 * iters + 2 passes for the subspace iteration
+    (R is re-formed from W, W0 and s on every pass), plus the band mean (n
+    weights read, W0 written); reported as GB/s against HBM."""
+    import torch
+    import rank_weight_reconstruction_wl_gb300 as wl
+    import wl_synth
+
+    hbm_peak, _, kind = load_peaks()
+    g = torch.Generator(device=dev)
+    g.manual_seed(23)
+    res = {"r": r, "p": p, "iters": iters, "layers_per_band": n, "peak_gbs": hbm_peak, "peak_kind": kind}
+    tot_ms, tot_b = 0.0, 0
+    for name, (inp, out) in (("q", (1152, 1024)), ("o", (1024, 1152)), ("gate", (1152, 6912)),
+                             ("down", (6912, 1152))):
+        Ws = [wl_synth.draw_theta(g, inp, out, 0).W0 for _ in range(n)]
+        wl.wl_decompose_band(Ws, r, p, iters, seed=1)  # warm-up
+        torch.cuda.synchronize(dev)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        reps = 3
+        for _ in range(reps):
+            wl.wl_decompose_band(Ws, r, p, iters, seed=1)
+        e1.record()
+        torch.cuda.synchronize(dev)
+        ms = e0.elapsed_time(e1) / reps
+        w = 2 * out * inp
+        b = (n + 1) * w + n * (2 * iters + 3) * 2 * w
+        res[name] = {"ms_per_band": round(ms, 3), "GBs": round(b / (ms * 1e-3) / 1e9, 1),
+                     "frac_of_hbm": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)}
+        tot_ms += ms
+        tot_b += b
+    res["all"] = {"ms": round(tot_ms, 3), "GBs": round(tot_b / (tot_ms * 1e-3) / 1e9, 1)}
     return res
 
 

@@ -180,6 +180,34 @@ wl_status wl_materialize(const void *W0, const float *s, const void *U, const vo
                          wl_out_dtype dt, void *stream);
 
 /*
+ * Decomposition of dense projection weights into theta bundles (the pages'
+ * weight adapter "auto-decomposes" a checkpoint into the bundle: "Serve and
+ * generate with weightless", "How the custom architecture loads").  One call
+ * handles one band: the n layers of one projection family that share a W0.
+ * Steps (the pages fix only the passthrough point G = num_layers, where each
+ * reconstructed weight equals the original; the rest is this library's
+ * reading):
+ *   W0 = mean of the n weights (fp32 sum, bf16 round-to-nearest-even);
+ *   s_l[o] = <W_l[o], W0[o]> / <W0[o], W0[o]> (1 where the W0 row is zero);
+ *   U_l, V_l: rank-r truncated SVD of R_l = W_l - diag(s_l) W0, split evenly
+ *   (U = U_r S^1/2, V = V_r S^1/2), by randomized subspace iteration from the
+ *   caller's Gaussian start omega [in, r + p] fp32 with `iters` power
+ *   iterations (Halko, Martinsson and Tropp 2011), then bf16.
+ * With n = 1 the bundle is the passthrough one: W0 = W, s = 1, U = V = 0.
+ * W: host array of n device pointers to bf16 [out, in] (16-byte aligned).
+ * Outputs (device, caller-owned): W0 bf16 [out, in]; s fp32 [n, out];
+ * U bf16 [n, out, r]; V bf16 [n, in, r].  workspace: at least
+ * wl_decompose_workspace_bytes(out, in, r, p) bytes, 256-byte aligned.
+ * Limits: 1 <= n <= 64, in % 8 == 0, 0 <= r <= min(out, in, 128),
+ * 0 <= p, r + p <= 160, 0 <= iters <= 64.  Asynchronous on `stream`.
+ */
+size_t wl_decompose_workspace_bytes(int64_t out, int64_t in, int64_t r, int64_t p);
+
+wl_status wl_decompose_band(const void *const *W, int64_t n, int64_t out, int64_t in, int64_t r,
+                            int64_t p, int64_t iters, const float *omega, void *W0, float *s,
+                            void *U, void *V, void *workspace, size_t ws_bytes, void *stream);
+
+/*
  * Decoder-layer stacks at decode size, in one launch per step.
  *
  * A weightless decoder layer applies its projections in a chain ("Serve and

@@ -22,7 +22,8 @@ import torch
 
 __all__ = [
     "WLError", "lib", "library_path", "wl_linear", "wl_qkv_fused", "wl_mlp_workspace_bytes",
-    "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_band_of_layer", "wl_device_status",
+    "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_decompose_band", "decompose",
+    "wl_band_of_layer", "wl_device_status",
     "wl_last_error", "wl_version", "wl_selftest_wait", "WLStack", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
     "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
 ]
@@ -37,7 +38,8 @@ STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3:
                 4: "WL_ERR_TIMEOUT", 5: "WL_ERR_WORKSPACE"}
 
 # Every function include/wl.h declares.
-EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_linear_f32", "wl_qkv_fused_f32", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
+EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_linear_f32", "wl_qkv_fused_f32", "wl_decompose_workspace_bytes",
+                    "wl_decompose_band", "wl_mlp_workspace_bytes", "wl_mlp_geglu_fused",
                     "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_stack_create", "wl_stack_decode",
                     "wl_stack_destroy", "wl_band_of_layer", "wl_device_status", "wl_last_error", "wl_version", "wl_selftest_wait")
 
@@ -94,6 +96,11 @@ def lib():
         L.wl_linear_f32.restype = st
         L.wl_qkv_fused_f32.argtypes = [vp, _ProjF32, _ProjF32, _ProjF32, vp, vp, vp, i64, i64, i64, C.c_int, vp]
         L.wl_qkv_fused_f32.restype = st
+        L.wl_decompose_workspace_bytes.argtypes = [i64, i64, i64, i64]
+        L.wl_decompose_workspace_bytes.restype = C.c_size_t
+        L.wl_decompose_band.argtypes = [C.POINTER(C.c_void_p), i64, i64, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp,
+                                        C.c_size_t, vp]
+        L.wl_decompose_band.restype = st
         L.wl_mlp_workspace_bytes.argtypes = [i64, i64, i64, i64, C.c_int]
         L.wl_mlp_workspace_bytes.restype = C.c_size_t
         L.wl_mlp_geglu_fused.argtypes = [vp, _Proj, _Proj, _Proj, vp, i64, i64, i64, i64, vp,
@@ -339,6 +346,57 @@ def wl_materialize(W0, s, U, V, dt=torch.bfloat16, out=None, stream=None):
         _check(lib().wl_materialize(p.W0, p.s, p.U, p.V, _ptr(out), o, inp, r, code,
                                     _stream(stream, W0.device)))
     return out
+
+
+def wl_decompose_band(Ws, r, p=8, iters=4, omega=None, seed=0, stream=None):
+    """The theta bundle of one band: Ws (list of n bf16 [out, in] weights of
+    one projection family, sharing one W0) -> (W0 [out, in] bf16, s [n, out]
+    fp32, U [n, out, r] bf16, V [n, in, r] bf16).  omega [in, r + p] fp32 is
+    the Gaussian start of the subspace iteration (drawn from `seed` when not
+    given).  The binding allocates the outputs and the workspace; the library
+    call allocates nothing."""
+    n = len(Ws)
+    out, inp = Ws[0].shape
+    dev = Ws[0].device
+    for i, W in enumerate(Ws):
+        _need(W, f"Ws[{i}]", torch.bfloat16, (out, inp))
+    k = r + p
+    if omega is None:
+        g = torch.Generator(device=dev)
+        g.manual_seed(int(seed))
+        omega = torch.randn(inp, k, generator=g, device=dev, dtype=torch.float32)
+    if r > 0:
+        _need(omega, "omega", torch.float32, (inp, k))
+    W0 = torch.empty(out, inp, dtype=torch.bfloat16, device=dev)
+    s = torch.empty(n, out, dtype=torch.float32, device=dev)
+    U = torch.empty(n, out, r, dtype=torch.bfloat16, device=dev)
+    V = torch.empty(n, inp, r, dtype=torch.bfloat16, device=dev)
+    # 0 for sizes the library rejects: the call below then reports why
+    nb = int(lib().wl_decompose_workspace_bytes(out, inp, r, p))
+    ws = torch.empty(nb + 256, dtype=torch.uint8, device=dev)
+    off = (-ws.data_ptr()) % 256
+    ptrs = (C.c_void_p * n)(*[W.data_ptr() for W in Ws])
+    with torch.cuda.device(dev):
+        _check(lib().wl_decompose_band(ptrs, n, out, inp, r, p, iters, _ptr(omega) if r > 0 else None, _ptr(W0),
+                                       _ptr(s), _ptr(U) if r > 0 else None, _ptr(V) if r > 0 else None,
+                                       C.c_void_p(ws.data_ptr() + off), nb, _stream(stream, dev)))
+    return W0, s, U, V
+
+
+def decompose(Ws, G, r, p=8, iters=4, seed=0, stream=None):
+    """Theta bundles of a family's L dense weights with G shared W0 blocks:
+    layer l uses block wl_band_of_layer(l, L, G).  Returns a list of L
+    (W0, s, U, V) tuples; layers of a band share their W0 tensor."""
+    L = len(Ws)
+    bands = [[] for _ in range(G)]
+    for l in range(L):
+        bands[wl_band_of_layer(l, L, G)].append(l)
+    res = [None] * L
+    for b, members in enumerate(bands):
+        W0, s, U, V = wl_decompose_band([Ws[l] for l in members], r, p, iters, seed=seed + b, stream=stream)
+        for j, l in enumerate(members):
+            res[l] = (W0, s[j], U[j], V[j])
+    return res
 
 
 class WLStack:

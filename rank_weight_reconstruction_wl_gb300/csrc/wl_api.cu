@@ -277,6 +277,43 @@ wl_status wl_materialize(const void *W0, const float *s, const void *U, const vo
                               static_cast<cudaStream_t>(stream));
 }
 
+size_t wl_decompose_workspace_bytes(int64_t out, int64_t in, int64_t r, int64_t p)
+{
+    if (out < 1 || in < 8 || in % 8 || out > kMaxDim || in > kMaxDim || r < 0 || p < 0 || r + p > kDecompMaxK)
+        return 0;
+    return decompose_workspace_bytes(out, in, r, p);
+}
+
+wl_status wl_decompose_band(const void *const *W, int64_t n, int64_t out, int64_t in, int64_t r, int64_t p,
+                            int64_t iters, const float *omega, void *W0, float *s, void *U, void *V,
+                            void *workspace, size_t ws_bytes, void *stream)
+{
+    t_err[0] = '\0';
+    if (!W || n < 1 || n > kDecompMaxLayers)
+        return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: need 1 <= n <= %d weights", kDecompMaxLayers);
+    WL_TRY(check_dims(1, in, out, r));
+    if (r > out || r > in) return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: r = %lld exceeds min(out, in)", (long long)r);
+    if (p < 0 || r + p > kDecompMaxK)
+        return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: need p >= 0 and r + p <= %d", kDecompMaxK);
+    if (iters < 0 || iters > 64) return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: need 0 <= iters <= 64");
+    for (int64_t l = 0; l < n; ++l)
+        if (!W[l] || !aligned(W[l], 16))
+            return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: weight %lld is NULL or not 16-byte aligned", (long long)l);
+    if (!W0 || !aligned(W0, 16) || !s || !aligned(s, 4))
+        return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: W0 (16-byte aligned) and s must not be NULL");
+    if (r > 0 && (!U || !V || !omega || !aligned(U, 2) || !aligned(V, 2) || !aligned(omega, 4)))
+        return fail(WL_ERR_INVALID_ARG, "wl_decompose_band: U, V and omega must not be NULL when r > 0");
+    if (!workspace || !aligned(workspace, 256))
+        return fail(WL_ERR_WORKSPACE, "wl_decompose_band: workspace must be non-NULL and 256-byte aligned");
+    const size_t need = decompose_workspace_bytes(out, in, r, p);
+    if (ws_bytes < need)
+        return fail(WL_ERR_WORKSPACE, "wl_decompose_band: workspace too small: %zu bytes, need %zu", ws_bytes, need);
+    WL_TRY(begin());
+    return launch_decompose(reinterpret_cast<const bf16 *const *>(W), (int)n, (int)out, (int)in, (int)r, (int)p,
+                            (int)iters, omega, static_cast<bf16 *>(W0), s, static_cast<bf16 *>(U),
+                            static_cast<bf16 *>(V), workspace, ws_bytes, static_cast<cudaStream_t>(stream));
+}
+
 int64_t wl_band_of_layer(int64_t layer, int64_t L, int64_t G)
 {
     if (L < 1 || G < 1 || G > L || layer < 0 || layer >= L) return -1;

@@ -129,6 +129,13 @@ int wide_stack_device(const WidePlan *pl);
 wl_status launch_f32_linear(const float *x, const wl_proj_f32 *proj, int nproj, void *const *y, int64_t T,
                             int64_t in, int64_t r, int ydt, cudaStream_t st);
 
+// Dense weights -> theta bundles, one band (decompose.cu)
+constexpr int kDecompMaxLayers = 64;
+constexpr int kDecompMaxK = 160;
+size_t decompose_workspace_bytes(int64_t out, int64_t in, int64_t r, int64_t p);
+wl_status launch_decompose(const bf16 *const *W, int n, int out, int in, int r, int p, int iters, const float *omega,
+                           bf16 *W0, float *s, bf16 *U, bf16 *V, void *ws, size_t ws_bytes, cudaStream_t st);
+
 wl_status launch_materialize(const bf16 *W0, const float *s, const bf16 *U,
                              const bf16 *V, void *W_eff, int64_t out, int64_t in,
                              int64_t r, int dt, cudaStream_t st);
