@@ -46,6 +46,7 @@
 // previous kernel to finish before reading its input or writing any output.
 #include <cooperative_groups.h>
 
+#include <algorithm>
 #include <mutex>
 #include <unordered_map>
 
@@ -125,15 +126,111 @@ __device__ __forceinline__ float warp_reduce8(const float v[8])
     return d;
 }
 
+// Coalesced x V for r = 8*RG ranks, RG a power of two up to 16 (16-byte
+// aligned V): a CTA's V slice [n][r] is one contiguous block, read as 16-byte
+// chunks with thread tid on rank group g = tid % RG (8 ranks) of rows
+// tid / RG, tid / RG + kThreads / RG, ...; a warp's loads then cover whole
+// 128-byte lines.  Returns RG, or 0 where the layout does not allow it.
+__device__ __forceinline__ int zlin_groups(const bf16 *V, int r)
+{
+    const int RG = r >> 3;
+    const bool ok = r > 0 && (r & 7) == 0 && RG <= 16 && (RG & (RG - 1)) == 0 &&
+                    (reinterpret_cast<uintptr_t>(V) & 15) == 0;
+    return ok ? RG : 0;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 u, float v[8])
+{
+    v[0] = bf_lo(u.x); v[1] = bf_hi(u.x); v[2] = bf_lo(u.y); v[3] = bf_hi(u.y);
+    v[4] = bf_lo(u.z); v[5] = bf_hi(u.z); v[6] = bf_lo(u.w); v[7] = bf_hi(u.w);
+}
+
+// p[t][e] += src(t, i) * V[i*r + 8g + e] over this thread's rows i in
+// [i0, i1) (lg = log2 RG); tid, nthr: this thread's index among the nthr
+// threads that share the work.
+template <int TT, int UR, typename Src>
+__device__ __forceinline__ void zlin_rows(Src src, const uint4 *__restrict__ Vq, int RG, int lg, int i0, int i1,
+                                          float p[TT][8], int tid, int nthr)
+{
+    const int g = tid & (RG - 1);
+#pragma unroll UR
+    for (int i = i0 + (tid >> lg); i < i1; i += nthr >> lg) {
+        float v[8];
+        unpack8(Vq[(int64_t)i * RG + g], v);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+            const float xv = src(t, i);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[t][e] = fmaf(xv, v[e], p[t][e]);
+        }
+    }
+}
+
+// out[t*ostride + 8g + e] = the sum of p[t][e] over the threads of rank group
+// g: a butterfly over the lanes of a group, then the warps' sums in a fixed
+// order through zred (512 floats), 64 ranks at a time.  Contains consumer
+// barriers.
+template <int TT>
+__device__ __forceinline__ void zlin_finish(float p[TT][8], int RG, int r, float *out, int ostride, float *zred)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int off = RG; off < 32; off <<= 1)
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[t][e] += __shfl_xor_sync(0xffffffffu, p[t][e], off);
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+        for (int kb = 0; kb < r; kb += 64) {
+            if (lane < RG && 8 * lane >= kb && 8 * lane < kb + 64)
+#pragma unroll
+                for (int e = 0; e < 8; ++e) zred[warp * 64 + 8 * lane - kb + e] = p[t][e];
+            consumer_sync();
+            if (threadIdx.x < min(64, r - kb)) {
+                float sum = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) sum += zred[w * 64 + threadIdx.x];
+                out[t * ostride + kb + threadIdx.x] = sum;
+            }
+            consumer_sync();
+        }
+}
+
+// One token, r <= 64 (RG <= 8): the warp's sums of p over the lanes of each
+// rank group, stored as part[8*g + e] (64 floats per warp).
+__device__ __forceinline__ void zlin_warp_store(float p[1][8], int RG, float *part)
+{
+    const int lane = threadIdx.x & 31;
+    for (int off = RG; off < 32; off <<= 1)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) p[0][e] += __shfl_xor_sync(0xffffffffu, p[0][e], off);
+    if (lane < RG)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) part[8 * lane + e] = p[0][e];
+}
+
 // out[t*ostride + k] = sum_{i < n} src(t, i) * V[i*r + k] for t < TT,
-// k < r (out may be shared or global memory).  One thread per row i of V,
-// eight ranks per load, several loads in flight per thread; partial sums are
-// reduced across the warp, then across warps in shared memory (zred:
-// kWarps*TT*8 floats).  Contains consumer barriers.
+// k < r (out may be shared or global memory).  The coalesced form above where
+// the layout allows it; otherwise one thread per row i of V, eight ranks per
+// load, partial sums reduced across the warp, then across warps in shared
+// memory (zred: 512 floats).  Contains consumer barriers.
 template <int TT, typename Src>
 __device__ __forceinline__ void block_xV(Src src, int n, const bf16 *__restrict__ V, int r,
                                          float *out, int ostride, float *zred)
 {
+    constexpr int UR = TT == 1 ? 8 : TT <= 2 ? 4 : 1;  // rows in flight (registers)
+    const int RG = zlin_groups(V, r);
+    if (RG) {
+        float p[TT][8];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[t][e] = 0.f;
+        zlin_rows<TT, UR>(src, reinterpret_cast<const uint4 *>(V), RG, __ffs(RG) - 1, 0, n, p, threadIdx.x,
+                          kThreads);
+        zlin_finish<TT>(p, RG, r, out, ostride, zred);
+        return;
+    }
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int vm = vec_mode(V, r);
     for (int kc = 0; kc < r; kc += 8) {
@@ -142,7 +239,7 @@ __device__ __forceinline__ void block_xV(Src src, int n, const bf16 *__restrict_
         for (int t = 0; t < TT; ++t)
 #pragma unroll
             for (int e = 0; e < 8; ++e) p[t][e] = 0.f;
-#pragma unroll 2
+#pragma unroll UR
         for (int i = tid; i < n; i += kThreads) {
             float v[8];
             load8(V, i, r, kc, vm, v);
@@ -178,7 +275,10 @@ template <int TT>
 __device__ __forceinline__ void add_delta(const bf16 *__restrict__ U, int64_t o, int r, int vm,
                                           const float *z, int zs, float yv[TT])
 {
-#pragma unroll 2
+    // at few tokens every rank group's load is issued before the first
+    // multiply (the loop is latency-bound: U is read once, cold)
+    constexpr int UR = TT <= 2 ? 8 : 2;
+#pragma unroll UR
     for (int kc = 0; kc < r; kc += 8) {
         float u[8];
         load8(U, o, r, kc, vm, u);
@@ -196,7 +296,7 @@ __device__ __forceinline__ void add_delta(const bf16 *__restrict__ U, int64_t o,
 struct Ring {
     char *base;       // nst stages of kStageBytes, 1024-byte aligned
     uint64_t *full;   // [nst]: producer -> consumers (transaction bytes)
-    uint64_t *empty;  // [nst]: consumers -> producer (kWarps arrivals)
+    uint64_t *empty;  // [nst]: consumers -> producer (one arrival per consumer warp)
     int nst;
     int s;            // current stage
     unsigned ph;      // parity of the current pass over the ring
@@ -236,18 +336,23 @@ __device__ __forceinline__ bool produce_tile(Ring &rg, const CUtensorMap *map, i
     return true;
 }
 
-// Consumers: the tile's stages on the tensor cores.  Warp w owns rows
-// 16*(w&3) .. +15 of the tile and the k-steps of parity (w>>2) of each stage;
-// the two warps of a row group are added at the end.  xb: the tile's x as
-// bf16 pairs, row n (token) at xb + n*xs32 (u32 units), column 0 = the CTA's
-// k0, zero past its K range.  acc[row*ald + n] receives the raw dot products
-// of the 64 rows with the 8*NT columns.  red: 512*NT floats.
-template <int NT>
-__device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_t *xb, int xs32,
+// Consumers: the tile's stages on the tensor cores.  KW = 2: warps 0-7, warp w
+// owns rows 16*(w&3) .. +15 of the tile and the k-steps of parity (w>>2) of
+// each stage; the two warps of a row group are added at the end (consumer
+// barriers).  KW = 1: warps 0-3 only, warp w owns rows 16*w .. +15 and all
+// eight k-steps of each stage (no barrier; the ring's empty barriers then
+// count four arrivals).  xb: the tile's x as
+// bf16 pairs, row n (token) at xb + n*xs32 (u32 units) for n < nx, column 0 =
+// the CTA's k0, zero past its K range; the MMA columns n >= nx are zeros that
+// are not stored (at one token x takes an eighth of the shared memory).
+// acc[row*ald + n] receives the raw dot products of the 64 rows with the 8*NT
+// columns.  red: 512*NT floats.
+template <int NT, int KW = 2>
+__device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_t *xb, int xs32, int nx,
                                              float *red, float *acc, int ald, unsigned *status)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rw = warp & 3, kw = warp >> 2;
+    const int rw = warp & 3, kw = KW == 2 ? warp >> 2 : 0;
     const int g = lane >> 2, t4 = lane & 3;
     float c[NT][4];
 #pragma unroll
@@ -267,12 +372,14 @@ __device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_
             break;
         }
         const uint32_t sb = smem_u32(rg.base + (size_t)rg.s * kStageBytes);
-        // the stage's fragments first (A of the four k steps of this warp, then
-        // their B words), then the MMAs
+        // the stage's fragments first (A of four k steps of this warp, then
+        // their B words), then the MMAs; KW = 1 takes two such passes
+#pragma unroll
+        for (int h = 0; h < 8 / KW; h += 4) {
         uint32_t a[4][4], bw[4][NT][2];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int step = kw + 2 * q;    // 0..7 within the stage
+            const int step = KW == 2 ? kw + 2 * q : h + q;  // 0..7 within the stage
             const int box = step >> 2;      // which 64-column box
             const int kin = step & 3;       // 16-column step inside the box
             if (kt + box >= ktiles) continue;
@@ -282,20 +389,33 @@ __device__ __forceinline__ bool consume_tile(Ring &rg, int ktiles, const uint32_
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 const uint32_t xa = xb_ln + (uint32_t)((nt * 8 * xs32 + (kk >> 1)) * 4);
-                bw[q][nt][0] = lds_u32(xa);
-                bw[q][nt][1] = lds_u32(xa + 16);
+                const bool v = nt * 8 + g < nx;
+                bw[q][nt][0] = v ? lds_u32(xa) : 0u;
+                bw[q][nt][1] = v ? lds_u32(xa + 16) : 0u;
             }
         }
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int box = (kw + 2 * q) >> 2;
+            const int box = (KW == 2 ? kw + 2 * q : h + q) >> 2;
             if (kt + box >= ktiles) continue;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_16816(c[nt], a[q], bw[q][nt][0], bw[q][nt][1]);
         }
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(&rg.empty[rg.s]);
         rg.advance();
+    }
+    if (KW == 1) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = rw * 16 + g, col = nt * 8 + 2 * t4;
+            acc[row * ald + col] = c[nt][0];
+            acc[row * ald + col + 1] = c[nt][1];
+            acc[(row + 8) * ald + col] = c[nt][2];
+            acc[(row + 8) * ald + col + 1] = c[nt][3];
+        }
+        return ok;
     }
     // add the two k-halves of every row group and store
     if (kw == 1) {
@@ -379,11 +499,12 @@ __device__ __forceinline__ Carve carve(char *smem_raw, int nst)
     return c;
 }
 
-__device__ __forceinline__ void init_barriers(Carve &c, int KS)
+// cw: consumer warps that release each ring stage
+__device__ __forceinline__ void init_barriers(Carve &c, int KS, int cw = kWarps)
 {
     for (int i = 0; i < c.rg.nst; ++i) {
         mbar_init(&c.rg.full[i], 1);
-        mbar_init(&c.rg.empty[i], kWarps);
+        mbar_init(&c.rg.empty[i], cw);
     }
     mbar_init(c.ex.ready, KS);
     mbar_init(c.ex.done, KS);
@@ -391,7 +512,7 @@ __device__ __forceinline__ void init_barriers(Carve &c, int KS)
 }
 
 // x[t, k0:k0+klen) (bf16, row stride ld) -> xb rows (bf16, xs32 u32 per row),
-// width 64*ktiles (zero past klen); rows t >= T zero.  nrow = 8*NT rows.
+// width 64*ktiles (zero past klen); rows T <= t < nrow zero.
 __device__ __forceinline__ void stage_x(const bf16 *__restrict__ x, int64_t ld, int T, int k0, int klen,
                                         int width, int nrow, uint32_t *xb, int xs32)
 {
@@ -430,7 +551,10 @@ struct DecArgs {
     unsigned *status;
 };
 
-template <int NT, int TC>
+// ZW (one token, r = 8*RG <= 64, RG a power of two, V 16-byte aligned):
+// warps 0-3 stream W0 while warps 4-7 form z = x V over the CTA's K range, so
+// the rank-r reads overlap the W0 stream instead of following it.
+template <int NT, int TC, bool ZW = false>
 __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid_constant__ DecArgs a)
 {
     extern __shared__ __align__(1024) char smem_raw[];
@@ -450,7 +574,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid
 
     Carve c = carve(smem_raw, a.nst);
     uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
-    float *acc = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *acc = reinterpret_cast<float *>(xb + a.T * a.xs32);  // x: T rows
     float *red = acc + a.tpc * kBR * ald;
     float *zp = red + 512 * NT;  // [ceil8(T)][rp]
     float *zred = zp + ((a.T + 7) / 8) * 8 * rp;
@@ -459,7 +583,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid
     char *ubuf = vbuf + a.vbuf;
 
     if (threadIdx.x == 0) {
-        init_barriers(c, KS);
+        init_barriers(c, KS, ZW ? 4 : kWarps);
         pdl_trigger();
     }
     __syncthreads();           // barriers initialised (this CTA)
@@ -479,23 +603,44 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid
     const bf16 *Vp = sg.V + (int64_t)k0 * a.r;
     const bf16 *Up = sg.U + (int64_t)r0 * a.r;
     if (a.r > 0 && a.vbuf > 0) {
-        Vp = reinterpret_cast<const bf16 *>(prefetch(vbuf, Vp, klen * a.r * 2));
+        if (!ZW) Vp = reinterpret_cast<const bf16 *>(prefetch(vbuf, Vp, klen * a.r * 2));
         Up = reinterpret_cast<const bf16 *>(prefetch(ubuf, Up, nrows * a.r * 2));
     }
     pdl_wait();  // x comes from the previous kernel on the stream
-    stage_x(a.x, a.in, a.T, k0, klen, ktiles * kBK, 8 * NT, xb, a.xs32);
-    consumer_sync();
-    // W0 first: the ring has been filling since the kernel started
-    for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
-        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, acc + tl * kBR * ald, ald, a.status);
-    cp_async_wait_all();
+    stage_x(a.x, a.in, a.T, k0, klen, ktiles * kBK, a.T, xb, a.xs32);
     consumer_sync();
     const bf16 *xbh = reinterpret_cast<const bf16 *>(xb);
     const int xsh = 2 * a.xs32;
+    if constexpr (ZW) {
+        const int warp = threadIdx.x >> 5;
+        const int RG = a.r >> 3;
+        if (warp < 4) {
+            for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
+                consume_tile<NT, 1>(c.rg, ktiles, xb, a.xs32, a.T, red, acc + tl * kBR * ald, ald, a.status);
+        } else {
+            float p[1][8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[0][e] = 0.f;
+            zlin_rows<1, 16>([&](int, int i) { return bf2f(xbh[i]); }, reinterpret_cast<const uint4 *>(Vp), RG,
+                             __ffs(RG) - 1, 0, klen, p, threadIdx.x - 128, 128);
+            zlin_warp_store(p, RG, zred + (warp - 4) * 64);
+        }
+        cp_async_wait_all();
+        consumer_sync();
+        for (int k = threadIdx.x; k < a.r; k += kThreads)
+            zp[k] = (zred[k] + zred[64 + k]) + (zred[128 + k] + zred[192 + k]);
+        consumer_sync();
+    } else {
+    // W0 first: the ring has been filling since the kernel started
+    for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, a.T, red, acc + tl * kBR * ald, ald, a.status);
+    cp_async_wait_all();
+    consumer_sync();
     if (a.r > 0)
         for (int t0 = 0; t0 < a.T; t0 += TC)
             block_xV<TC>([&](int t, int i) { return t0 + t < a.T ? bf2f(xbh[(t0 + t) * xsh + i]) : 0.f; },
                          klen, Vp, a.r, zp + t0 * rp, rp, zred);
+    }
 
     // epilogue: p = s*acc + U z_range
     const int vmU = vec_mode(Up, a.r);
@@ -550,7 +695,9 @@ struct GateUpArgs {
     unsigned *status;
 };
 
-template <int TC>
+// ZW: as for dec_linear_kernel (warps 4-7 form z_gate and z_up while warps
+// 0-3 stream the gate and up tiles).
+template <int TC, bool ZW = false>
 __global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid_constant__ GateUpArgs a)
 {
     constexpr int NT = 1, ald = 8;
@@ -568,7 +715,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid
 
     Carve c = carve(smem_raw, a.nst);
     uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
-    float *accg = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *accg = reinterpret_cast<float *>(xb + a.T * a.xs32);  // x: T rows
     float *accu = accg + a.tpc * kBR * ald;
     float *red = accu + a.tpc * kBR * ald;
     float *zg = red + 512 * NT;   // [8][rp]
@@ -584,7 +731,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid
     char *vdb = uub + a.ubuf;
 
     if (threadIdx.x == 0) {
-        init_barriers(c, KS);
+        init_barriers(c, KS, ZW ? 4 : kWarps);
         pdl_trigger();
     }
     __syncthreads();           // barriers initialised (this CTA)
@@ -608,27 +755,60 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_gateup_kernel(const __grid
     const bf16 *Ugp = a.Ug + (int64_t)j0 * a.r, *Uup = a.Uu + (int64_t)j0 * a.r;
     const bf16 *Vdp = a.Vd + (int64_t)(j0 + lo) * a.r;
     if (a.r > 0 && a.vbuf > 0 && a.dbuf > 0) {
-        Vgp = reinterpret_cast<const bf16 *>(prefetch(vgb, Vgp, klen * a.r * 2));
-        Vup = reinterpret_cast<const bf16 *>(prefetch(vub, Vup, klen * a.r * 2));
+        if (!ZW) {
+            Vgp = reinterpret_cast<const bf16 *>(prefetch(vgb, Vgp, klen * a.r * 2));
+            Vup = reinterpret_cast<const bf16 *>(prefetch(vub, Vup, klen * a.r * 2));
+        }
         Ugp = reinterpret_cast<const bf16 *>(prefetch(ugb, Ugp, nr * a.r * 2));
         Uup = reinterpret_cast<const bf16 *>(prefetch(uub, Uup, nr * a.r * 2));
         Vdp = reinterpret_cast<const bf16 *>(prefetch(vdb, Vdp, n * a.r * 2));
     }
     pdl_wait();
-    stage_x(a.x, a.hidden, a.T, k0, klen, ktiles * kBK, 8 * NT, xb, a.xs32);
-    consumer_sync();
-    for (int tl = 0; tl < ntl && ktiles > 0; ++tl) {
-        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, accg + tl * kBR * ald, ald, a.status);
-        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, accu + tl * kBR * ald, ald, a.status);
-    }
-    cp_async_wait_all();
+    stage_x(a.x, a.hidden, a.T, k0, klen, ktiles * kBK, a.T, xb, a.xs32);
     consumer_sync();
     const bf16 *xbh = reinterpret_cast<const bf16 *>(xb);
     const int xsh = 2 * a.xs32;
     auto xsrc = [&](int t, int i) { return t < a.T ? bf2f(xbh[t * xsh + i]) : 0.f; };
-    if (a.r > 0) {
-        block_xV<TC>(xsrc, klen, Vgp, a.r, zg, rp, zred);
-        block_xV<TC>(xsrc, klen, Vup, a.r, zu, rp, zred);
+    if constexpr (ZW) {
+        const int warp = threadIdx.x >> 5;
+        const int RG = a.r >> 3;
+        if (warp < 4) {
+            for (int tl = 0; tl < ntl && ktiles > 0; ++tl) {
+                consume_tile<NT, 1>(c.rg, ktiles, xb, a.xs32, a.T, red, accg + tl * kBR * ald, ald, a.status);
+                consume_tile<NT, 1>(c.rg, ktiles, xb, a.xs32, a.T, red, accu + tl * kBR * ald, ald, a.status);
+            }
+        } else {
+            auto x1 = [&](int, int i) { return bf2f(xbh[i]); };
+            float p[1][8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[0][e] = 0.f;
+            zlin_rows<1, 16>(x1, reinterpret_cast<const uint4 *>(Vgp), RG, __ffs(RG) - 1, 0, klen, p,
+                             threadIdx.x - 128, 128);
+            zlin_warp_store(p, RG, zred + (warp - 4) * 64);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) p[0][e] = 0.f;
+            zlin_rows<1, 16>(x1, reinterpret_cast<const uint4 *>(Vup), RG, __ffs(RG) - 1, 0, klen, p,
+                             threadIdx.x - 128, 128);
+            zlin_warp_store(p, RG, zred + 256 + (warp - 4) * 64);
+        }
+        cp_async_wait_all();
+        consumer_sync();
+        for (int k = threadIdx.x; k < a.r; k += kThreads) {
+            zg[k] = (zred[k] + zred[64 + k]) + (zred[128 + k] + zred[192 + k]);
+            zu[k] = (zred[256 + k] + zred[320 + k]) + (zred[384 + k] + zred[448 + k]);
+        }
+        consumer_sync();
+    } else {
+        for (int tl = 0; tl < ntl && ktiles > 0; ++tl) {
+            consume_tile<NT>(c.rg, ktiles, xb, a.xs32, a.T, red, accg + tl * kBR * ald, ald, a.status);
+            consume_tile<NT>(c.rg, ktiles, xb, a.xs32, a.T, red, accu + tl * kBR * ald, ald, a.status);
+        }
+        cp_async_wait_all();
+        consumer_sync();
+        if (a.r > 0) {
+            block_xV<TC>(xsrc, klen, Vgp, a.r, zg, rp, zred);
+            block_xV<TC>(xsrc, klen, Vup, a.r, zu, rp, zred);
+        }
     }
     // partial g, u over this K range: s*acc + U z_range (in place)
     const int vmUg = vec_mode(Ugp, a.r), vmUu = vec_mode(Uup, a.r);
@@ -716,7 +896,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
 
     Carve c = carve(smem_raw, a.nst);
     uint32_t *xb = reinterpret_cast<uint32_t *>(c.rest);
-    float *acc = reinterpret_cast<float *>(xb + 8 * NT * a.xs32);
+    float *acc = reinterpret_cast<float *>(xb + 2 * a.T * a.xs32);  // x: 2T rows (hi, lo)
     float *red = acc + a.tpc * kBR * ald;
     float *zp = red + 512 * NT;    // [8][rp]
     float *zred = zp + 8 * rp;     // [kThreads]
@@ -738,7 +918,9 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
     }
 
     // ------------------------------------------------ consumer warps
-    const int rr = (q == 0) ? a.r : 0;  // the low-rank term is added by one rank
+    // every CTA of a K split forms z_down; the low-rank term of a row is added
+    // by the CTA that stores the row
+    const int rr = a.r;
     const float *sdp = reinterpret_cast<const float *>(prefetch(sbuf, a.sd + o0, nr * 4));
     const bf16 *Udp = a.Ud + (int64_t)o0 * a.r;
     if (rr > 0 && a.ubuf > 0) Udp = reinterpret_cast<const bf16 *>(prefetch(ubuf, Udp, nr * a.r * 2));
@@ -748,11 +930,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
         const int nq = width >> 2;  // 4-column groups
         bf16 *xbh = reinterpret_cast<bf16 *>(xb);
         const int xsh = 2 * a.xs32;
-        for (int idx = threadIdx.x; idx < 8 * NT * nq; idx += kThreads) {
+        for (int idx = threadIdx.x; idx < 2 * a.T * nq; idx += kThreads) {
             const int n = idx / nq, cq = idx - n * nq;
             const int t = n < a.T ? n : n - a.T;
             float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (n < 2 * a.T && 4 * cq < klen)
+            if (4 * cq < klen)
                 v = __ldcg(reinterpret_cast<const float4 *>(a.h + (int64_t)t * a.inter + k0 + 4 * cq));
             const float e[4] = {v.x, v.y, v.z, v.w};
             for (int j = 0; j < 4; ++j) {
@@ -762,17 +944,47 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
         }
     }
     const int vmU = vec_mode(Udp, a.r);
-    // z_down[t][k] = sum over the nzd partials in a fixed order: threads split
-    // the partials into chunks (loads in flight together), chunk sums are then
-    // added in chunk order.
+    // z_down[t][k] = sum over the nzd partials in a fixed order.  One token,
+    // r = 4*RQ <= 64 (RQ a power of two): thread tid adds 16-byte chunk
+    // tid % RQ of partials tid / RQ, tid / RQ + kThreads / RQ, ... (sixteen
+    // loads in flight), then the lanes of a chunk and the warps are added in a
+    // fixed order (red is free before the W0 stream).  Otherwise threads split
+    // the partials into chunks of scalar loads, added in chunk order.
     const int nout = TC * rr;
-    if (nout > 0 && nout <= kThreads) {
+    const int RQ = rr >> 2;
+    if (TC == 1 && rr > 0 && (rr & 3) == 0 && rr <= 64 && (RQ & (RQ - 1)) == 0) {
+        const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, lq = __ffs(RQ) - 1;
+        const int g4 = threadIdx.x & (RQ - 1);
+        float4 sm = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 16
+        for (int p = threadIdx.x >> lq; p < a.nzd; p += kThreads >> lq) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(a.zd + (int64_t)p * kTokChunk * rp) + g4);
+            sm.x += v.x;
+            sm.y += v.y;
+            sm.z += v.z;
+            sm.w += v.w;
+        }
+        for (int off = RQ; off < 32; off <<= 1) {
+            sm.x += __shfl_xor_sync(0xffffffffu, sm.x, off);
+            sm.y += __shfl_xor_sync(0xffffffffu, sm.y, off);
+            sm.z += __shfl_xor_sync(0xffffffffu, sm.z, off);
+            sm.w += __shfl_xor_sync(0xffffffffu, sm.w, off);
+        }
+        if (lane < RQ) reinterpret_cast<float4 *>(red + warp * 64)[lane] = sm;
+        consumer_sync();
+        for (int k = threadIdx.x; k < rr; k += kThreads) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += red[w * 64 + k];
+            zp[k] = v;
+        }
+    } else if (nout > 0 && nout <= kThreads) {
         const int nch = kThreads / nout;
         const int ch = threadIdx.x / nout, cc = threadIdx.x - ch * nout;
         if (ch < nch) {
             const int t = cc / rr, k = cc - t * rr;
             float s = 0.f;
-#pragma unroll 4
+#pragma unroll 16
             for (int p = ch; p < a.nzd; p += nch) s += __ldcg(a.zd + ((int64_t)p * kTokChunk + t) * rp + k);
             zred[ch * nout + cc] = s;
         }
@@ -794,7 +1006,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
     cp_async_wait_all();
     consumer_sync();
     for (int tl = 0; tl < ntl && ktiles > 0; ++tl)
-        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, red, acc + tl * kBR * ald, ald, a.status);
+        consume_tile<NT>(c.rg, ktiles, xb, a.xs32, 2 * a.T, red, acc + tl * kBR * ald, ald, a.status);
     for (int row = threadIdx.x; row < nr; row += kThreads) {
         const int o = o0 + row;
         const float sv = sdp[row];
@@ -802,7 +1014,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
 #pragma unroll
         for (int t = 0; t < TC; ++t)
             yv[t] = (ktiles > 0 && t < a.T) ? sv * (acc[row * ald + t] + acc[row * ald + a.T + t]) : 0.f;
-        if (rr > 0) add_delta<TC>(Udp, row, rr, vmU, zp, rp, yv);
+        if (rr > 0 && KS == 1) add_delta<TC>(Udp, row, rr, vmU, zp, rp, yv);
 #pragma unroll
         for (int t = 0; t < TC; ++t) {
             if (t >= a.T) break;
@@ -821,6 +1033,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_down_kernel(const __grid_c
             const int t = idx / n, row = lo + (idx - t * n);
             float v = 0.f;
             for (int p = 0; p < KS; ++p) v += cl.map_shared_rank(acc, p)[row * ald + t];
+            if (rr > 0) add_delta<1>(Udp, row, rr, vmU, zp + t * rp, rp, &v);
             store_out(a.y, a.ydt, (int64_t)t * a.hidden + o0 + row, v);
         }
         exchange_release(c.ex, KS);
@@ -846,6 +1059,21 @@ static dec_fn g_dec[2][4] = {{dec_linear_kernel<1, 1>, nullptr, nullptr, nullptr
                              {dec_linear_kernel<1, 8>, dec_linear_kernel<2, 8>, dec_linear_kernel<4, 8>,
                               dec_linear_kernel<8, 8>}};
 static gu_fn g_gu[2] = {dec_gateup_kernel<1>, dec_gateup_kernel<8>};
+// one token with separate x V warps
+static dec_fn g_dec_zw = dec_linear_kernel<1, 1, true>;
+static gu_fn g_gu_zw = dec_gateup_kernel<1, true>;
+
+// The ZW forms apply: one token, r = 8*RG <= 64 with RG a power of two, every
+// V 16-byte aligned.
+static bool zw_ok(int64_t T, int64_t r, const void *const *V, int nv)
+{
+    if (T != 1 || r <= 0 || r > 64 || r % 8) return false;
+    const int RG = (int)(r / 8);
+    if (RG & (RG - 1)) return false;
+    for (int j = 0; j < nv; ++j)
+        if (reinterpret_cast<uintptr_t>(V[j]) % 16) return false;
+    return true;
+}
 static dn_fn g_dn[2][2] = {{dec_down_kernel<1, 1>, nullptr}, {dec_down_kernel<1, 8>, dec_down_kernel<2, 8>}};
 
 static inline int nt_index(int nt) { return nt <= 1 ? 0 : nt <= 2 ? 1 : nt <= 4 ? 2 : 3; }
@@ -889,7 +1117,7 @@ static wl_status launch(const void *fn, int grid, int KS, int smem, cudaStream_t
     return WL_OK;
 }
 
-// Work split of `ntile` 64-row tiles with K = in (see plan_balanced):
+// Work split of a launch's 64-row tiles with K = in (see plan_balanced):
 //   tpc   tiles per row group: each group forms z = x V once, so more tiles
 //         per group keep the rank-r operand's traffic small next to W0;
 //   KS    K splits (cluster size);
@@ -965,33 +1193,63 @@ static int cluster_capacity(const void *fn, int ks, int smem, const DeviceInfo *
     return cap;
 }
 
-// The split of `ntile` 64-row tiles by `in` columns among CTAs with the least
-// work on the busiest SM.  A row group of tpc tiles and a K split of Kc
-// columns make one CTA; its work is its W0 stream plus its V slice (r_eff
-// ranks) plus a fixed cost per CTA, in units of 64 x 1 tile columns.  CTAs
-// beyond what can be resident at once (cluster placement included), or
-// beyond one per SM, run as further rounds on the same SMs.  smem_of(tpc, Kc)
-// gives the launch's shared memory (< 0: does not fit).
+// Expected time of a launch plan, in microseconds, from a model calibrated on
+// GB300 decode timings (T = 1, forced plans):
+//   * a CTA keeps its ring's stages in flight, one round trip of a 16 KB stage
+//     taking about kStageLatUs, so an SM streams at min(its share of HBM,
+//     stages resident on it * 16 KB / kStageLatUs);
+//   * CTAs beyond one per SM share that SM's stream; beyond what can be
+//     resident at once (cluster placement included) they run as further
+//     rounds;
+//   * a K split costs a cluster exchange, about 0.7 us per split;
+//   * x V that follows the stream reads the V slice at about 40 GB/s per CTA;
+//     formed by four separate warps during the stream (zw) it runs at about
+//     12 GB/s and costs only what the stream does not hide;
+//   * clusters of 5, 7 or 8 CTAs place unevenly on the GPCs and measured far
+//     slower than this predicts; they are not used.
+constexpr double kHbmBytesPerUs = 6.8e6;
+constexpr double kStageLatUs = 2.34;
+constexpr double kZBytesPerUs = 4.0e4;    // x V after the stream, 8 warps
+constexpr double kZwBytesPerUs = 1.2e4;   // x V by 4 warps during the stream
+
+// The split of the segments' 64-row tiles (seg_tiles[0..nseg)) by `in` columns
+// with the least expected time.  A row group of tpc tiles of one segment and a
+// K split of Kc columns make one CTA, which streams pair*tpc tiles (gate and
+// up: pair = 2) and reads nzv V slices of r ranks.  smem_of(tpc, Kc, &nst)
+// gives the launch's shared memory and ring stages (< 0: does not fit).
 template <class SmemOf>
-static bool plan_balanced(int ntile, int in, int r_eff, int max_kc, int tpc_max, int max_ctas, const void *fn,
-                          SmemOf smem_of, const DeviceInfo *di, Split *out)
+static bool plan_balanced(const int *seg_tiles, int nseg, int in, int r, int pair, int nzv, bool zw, int max_kc,
+                          int tpc_max, int max_ctas, const void *fn, SmemOf smem_of, const DeviceInfo *di,
+                          Split *out)
 {
     double best = 1e30;
     int best_ctas = 0;
     bool found = false;
+    const int S = di->sm_count;
     for (int tpc = 1; tpc <= tpc_max; ++tpc) {
-        const int ngrp = cdiv(ntile, tpc);
-        for (int ks = 1; ks <= 8; ++ks) {
+        int ngrp = 0;
+        for (int j = 0; j < nseg; ++j) ngrp += cdiv(seg_tiles[j], tpc);
+        for (int ks = 1; ks <= 6; ++ks) {
+            if (ks == 5) continue;
             const int Kc = round_up(cdiv(in, ks), kBK);
             if (Kc > max_kc || cdiv(in, Kc) != ks) continue;
             const int ctas = ngrp * ks;
             if (ctas > max_ctas) continue;
-            const int smem = smem_of(tpc, Kc);
+            int nst = 0;
+            const int smem = smem_of(tpc, Kc, &nst);
             if (smem < 0) continue;
             const int cap = cluster_capacity(fn, ks, smem, di);
             if (cap <= 0) continue;
-            const int usable = cap < di->sm_count ? cap : di->sm_count;
-            const double cost = (double)cdiv(ctas, usable) * ((tpc + r_eff / 64.0) * Kc + 512.0);
+            const int res = ctas < cap ? ctas : cap;
+            const int rounds = cdiv(ctas, cap);
+            const int k = cdiv(res, S);
+            const int busy = res < S ? res : S;
+            const double bw = (double)pair * tpc * kBR * Kc * 2;
+            const double rate = std::min(kHbmBytesPerUs / busy, (double)k * nst * kStageBytes / kStageLatUs);
+            const double t_stream = k * bw / rate;
+            const double vb = (double)nzv * Kc * r * 2;
+            const double t_z = r <= 0 ? 0.0 : zw ? std::max(0.0, vb / kZwBytesPerUs - t_stream) : vb / kZBytesPerUs;
+            const double cost = rounds * (t_stream + t_z) + (ks > 1 ? 0.7 * ks : 0.0) + 1.0;
             if (cost < best * 0.999 || (cost < best * 1.001 && ctas < best_ctas)) {
                 best = cost;
                 best_ctas = ctas;
@@ -1021,25 +1279,31 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
 {
     wl_status s = WL_OK;
     const int NT = nt_round(cdiv(T, 8));
-    int ntile = 0;
-    for (int j = 0; j < nproj; ++j) ntile += cdiv(proj[j].out, kBR);
-    // keep x (8*NT rows of K columns) within about 48 KB; where the staged x
+    // keep x (T rows of K columns) within about 48 KB; where the staged x
     // and the per-tile partial sums still leave no room for two ring stages
     // (many tokens, long K, large rank), take fewer tiles per row group and
     // narrower K splits
-    int max_kc = (48 * 1024) / (8 * NT * 2);
+    int max_kc = (48 * 1024) / ((int)T * 2);
     max_kc = max_kc < kBK ? kBK : (max_kc / kBK) * kBK;
     const int rp0 = r > 0 ? (int)r : 1;
-    const dec_fn fn = g_dec[T == 1 ? 0 : 1][nt_index(NT)];
+    const void *vs[3] = {};
+    int seg_tiles[3] = {};
+    for (int j = 0; j < nproj; ++j) {
+        vs[j] = proj[j].V;
+        seg_tiles[j] = cdiv(proj[j].out, kBR);
+    }
+    const bool zw = zw_ok(T, r, vs, nproj);
+    const dec_fn fn = zw ? g_dec_zw : g_dec[T == 1 ? 0 : 1][nt_index(NT)];
     // shared memory of a (tpc, Kc) plan, as laid out below
-    auto smem_of = [&](int tpc, int Kc) {
+    auto smem_of = [&](int tpc, int Kc, int *nst_out) {
         const int xs = x_stride32(Kc);
         int pre = 0;
         const int vb = round_up(Kc * (int)r * 2 + 16, 16), ub = round_up(tpc * kBR * (int)r * 2 + 16, 16);
         if (r > 0 && vb + ub <= kPrefetchBudget) pre = vb + ub;
-        const int other = 8 * NT * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp0 + 512) +
+        const int other = (int)T * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp0 + 512) +
                           tpc * kBR * 4 + 16 + pre;
         const int nst = ring_stages(other, di);
+        *nst_out = nst;
         return nst < 2 ? -1 : carve_head_bytes(nst) + other;
     };
     s = ensure_attrs((const void *)fn, 0, di);
@@ -1047,12 +1311,14 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     Split sp;
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
-        const uint64_t key = plan_key(1, di->device, ntile, in, r, T);
+        const uint64_t key = plan_key(1, di->device, ((int64_t)seg_tiles[0] << 40) ^ ((int64_t)seg_tiles[1] << 20) ^ seg_tiles[2],
+                                      in, r, T * 2 + (zw ? 1 : 0));
         auto it = g_plans.find(key);
         if (it != g_plans.end()) {
             sp = it->second;
         } else {
-            if (!plan_balanced(ntile, (int)in, (int)r, max_kc, 8, 1 << 20, (const void *)fn, smem_of, di, &sp))
+            if (!plan_balanced(seg_tiles, nproj, (int)in, (int)r, 1, 1, zw, max_kc, 8, 1 << 20, (const void *)fn,
+                               smem_of, di, &sp))
                 return fail(WL_ERR_UNSUPPORTED, "decode: shapes too large for shared memory");
             g_plans[key] = sp;
         }
@@ -1091,7 +1357,7 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
         a.vbuf = vb;
         a.ubuf = ub;
     }
-    const int other = 8 * NT * a.xs32 * 4 + 4 * (sp.tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp + 512) +
+    const int other = (int)T * a.xs32 * 4 + 4 * (sp.tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp + 512) +
                       sp.tpc * kBR * 4 + 16 + a.vbuf + a.ubuf;
     a.nst = ring_stages(other, di);
     const int smem = carve_head_bytes(a.nst) + other;
@@ -1142,31 +1408,36 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
 
     // launch 1: gate and up tiles, h, partials of h V_down
     GateUpArgs g = {};
-    const gu_fn gfn = g_gu[T == 1 ? 0 : 1];
+    const void *gv[2] = {gate.V, up.V};
+    const bool gzw = zw_ok(T, r, gv, 2);
+    const gu_fn gfn = gzw ? g_gu_zw : g_gu[T == 1 ? 0 : 1];
     wl_status s = ensure_attrs((const void *)gfn, 0, di);
     if (s != WL_OK) return s;
     // shared memory of a gate/up plan (tpc, Kc), as laid out below
-    auto gsmem_of = [&](int tpc, int Kc) {
+    auto gsmem_of = [&](int tpc, int Kc, int *nst_out) {
         const int ks = cdiv(hidden, Kc);
         const int xs = x_stride32(Kc), hmax = cdiv(tpc * kBR, ks) + 1;
         const int vb = round_up(Kc * r * 2 + 16, 16), ub = round_up(tpc * kBR * r * 2 + 16, 16);
         const int db = round_up(hmax * r * 2 + 16, 16);
         const int pre = (r > 0 && 2 * vb + 2 * ub + db <= kPrefetchBudget) ? 2 * vb + 2 * ub + db : 0;
-        const int other = 8 * xs * 4 + 4 * (2 * tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * hmax) +
+        const int other = T * xs * 4 + 4 * (2 * tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * hmax) +
                           2 * (tpc * kBR * 4 + 16) + pre;
         const int nst = ring_stages(other, di);
+        *nst_out = nst;
         return nst < 2 ? -1 : carve_head_bytes(nst) + other;
     };
     Split sg;
     {
         std::lock_guard<std::mutex> lk(g_plan_mu);
-        const uint64_t key = plan_key(2, di->device, inter, hidden, r, T);
+        const uint64_t key = plan_key(2, di->device, inter, hidden, r, T * 2 + (gzw ? 1 : 0));
         auto it = g_plans.find(key);
         if (it != g_plans.end()) {
             sg = it->second;
         } else {
             // gate and up tiles are a pair per CTA: twice the W0 stream and rank work per tile
-            if (!plan_balanced(cdiv(inter, kBR), hidden, 2 * r, 48 * 1024 / 16, 8, kMaxPartials, (const void *)gfn,
+            const int gt = cdiv(inter, kBR);
+            if (!plan_balanced(&gt, 1, hidden, r, 2, 2, gzw, 48 * 1024 / (2 * T) / kBK * kBK, 8, kMaxPartials,
+                               (const void *)gfn,
                                gsmem_of, di, &sg))
                 return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
             g_plans[key] = sg;
@@ -1205,7 +1476,7 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
             g.dbuf = db;
         }
     }
-    const int gother = 8 * g.xs32 * 4 + 4 * (2 * sg.tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * g.hmax) +
+    const int gother = T * g.xs32 * 4 + 4 * (2 * sg.tpc * kBR * 8 + 512 + 16 * rp + 512 + 8 * g.hmax) +
                        2 * (sg.tpc * kBR * 4 + 16) + 2 * g.vbuf + 2 * g.ubuf + g.dbuf;
     g.nst = ring_stages(gother, di);
     if (g.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
@@ -1222,12 +1493,13 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
     s = ensure_attrs((const void *)dfn, 0, di);
     if (s != WL_OK) return s;
-    auto dsmem_of = [&](int tpc, int Kc) {
+    auto dsmem_of = [&](int tpc, int Kc, int *nst_out) {
         const int xs = x_stride32(Kc);
         const int ub = round_up(tpc * kBR * r * 2 + 16, 16);
         const int pre = (r > 0 && ub <= kPrefetchBudget) ? ub : 0;
-        const int other = 8 * NT * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) + tpc * kBR * 4 + 16 + pre;
+        const int other = 2 * T * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) + tpc * kBR * 4 + 16 + pre;
         const int nst = ring_stages(other, di);
+        *nst_out = nst;
         return nst < 2 ? -1 : carve_head_bytes(nst) + other;
     };
     Split sd;
@@ -1238,7 +1510,8 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
         if (it != g_plans.end()) {
             sd = it->second;
         } else {
-            if (!plan_balanced(cdiv(hidden, kBR), inter, r, (48 * 1024) / (8 * NT * 2) / kBK * kBK, 8, 1 << 20,
+            const int dt = cdiv(hidden, kBR);
+            if (!plan_balanced(&dt, 1, inter, r, 1, 0, false, (48 * 1024) / (2 * T * 2) / kBK * kBK, 8, 1 << 20,
                                (const void *)dfn, dsmem_of, di, &sd))
                 return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
             g_plans[key] = sd;
@@ -1266,7 +1539,7 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
         const int ub = round_up(sd.tpc * kBR * r * 2 + 16, 16);
         if (r > 0 && ub <= kPrefetchBudget) d.ubuf = ub;
     }
-    const int dother = 8 * NT * d.xs32 * 4 + 4 * (sd.tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) +
+    const int dother = 2 * T * d.xs32 * 4 + 4 * (sd.tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) +
                        sd.tpc * kBR * 4 + 16 + d.ubuf;
     d.nst = ring_stages(dother, di);
     if (d.nst < 2) return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
