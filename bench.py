@@ -565,12 +565,13 @@ def unique_bytes(shapes, L, G, T, r):
     return b
 
 
-def measure_stack_grid(dev, steps=20, Ts=(1, 32), Gs=(L_LAYERS, 1), ranks=(4, 16, 32)):
+def measure_stack_grid(dev, steps=20, Ts=(1, 32), Gs=(L_LAYERS, 1), ranks=(4, 16, 32), nlayers=L_LAYERS):
     """The 26-layer stack on the stack engine over T (1: one request; 32: 32
     requests decoded together), G (26: one W0 per layer, every step streams
     1.4 GB of distinct weights; 1: one shared W0 set of 53.7 MB, which may stay
     in L2) and r.  Streamed bytes count every layer's W0 read (the algorithmic
-    bytes of the step); unique bytes count a shared W0 once."""
+    bytes of the step); unique bytes count a shared W0 once.  nlayers < 26 is
+    for profiling only (G = 26 then means one W0 per layer)."""
     import torch
     from rank_weight_reconstruction_wl_gb300.stack import DecoderStack, build_layers
 
@@ -580,7 +581,8 @@ def measure_stack_grid(dev, steps=20, Ts=(1, 32), Gs=(L_LAYERS, 1), ranks=(4, 16
     for T in Ts:
         for G in Gs:
             for r in ranks:
-                layers = build_layers(L_LAYERS, G, T, SHAPES, r, seed=17 + r, device=dev)
+                G_ = min(G, nlayers)
+                layers = build_layers(nlayers, G_, T, SHAPES, r, seed=17 + r, device=dev)
                 st = DecoderStack(layers, T, SHAPES["hidden"], SHAPES["q"], SHAPES["inter"], r, device=dev,
                                   engine="stack")
                 gx = torch.Generator(device=dev)
@@ -597,18 +599,18 @@ def measure_stack_grid(dev, steps=20, Ts=(1, 32), Gs=(L_LAYERS, 1), ranks=(4, 16
                 e1.record(st.stream)
                 st.stream.synchronize()
                 ms = e0.elapsed_time(e1) / steps
-                streamed = layer_bytes(SHAPES, T, r) * L_LAYERS
-                uniq = unique_bytes(SHAPES, L_LAYERS, G, T, r)
+                streamed = layer_bytes(SHAPES, T, r) * nlayers
+                uniq = unique_bytes(SHAPES, nlayers, G_, T, r)
                 gbs = streamed / (ms * 1e-3) / 1e9
                 out[f"T{T}_G{G}_r{r}"] = {
                     "ms_per_step": round(ms, 4),
                     "us_per_token_per_stack": round(ms * 1e3 / T, 3),
-                    "us_per_token_per_layer": round(ms * 1e3 / (T * L_LAYERS), 4),
+                    "us_per_token_per_layer": round(ms * 1e3 / (T * nlayers), 4),
                     "streamed_MB": round(streamed / 1e6, 1), "GBs_streamed": round(gbs, 1),
                     "frac_of_hbm_streamed": round(gbs / hbm_peak, 4),
                     "unique_MB": round(uniq / 1e6, 1),
                     "GBs_unique": round(uniq / (ms * 1e-3) / 1e9, 1),
-                    "tflops": round(layer_flops(SHAPES, T, r) * L_LAYERS / (ms * 1e-3) / 1e12, 2)}
+                    "tflops": round(layer_flops(SHAPES, T, r) * nlayers / (ms * 1e-3) / 1e12, 2)}
                 del st, layers
                 torch.cuda.empty_cache()
     return out
@@ -763,12 +765,13 @@ def measure_decompose(dev, r=16, p=8, iters=4, n=2):
 LARGE = dict(hidden=5376, q=4096, kv=2048, inter=21504, r=64)
 
 
-def measure_large(dev, nsets=2):
+def measure_large(dev, nsets=2, Ts=(1, 64, 4096), reps_small=10):
     """The large projection set (hidden 5376, intermediate 21504, Q/K/V
     5376 -> 4096/2048/2048, r = 64): fused Q/K/V and fused MLP calls at 1, 64
     and 4096 tokens, rotating over `nsets` weight sets (1.56 GB, larger than
     L2), timed by CUDA-graph replay.  GB/s of algorithmic bytes at 1 and 64
-    tokens, TFLOP/s at 4096."""
+    tokens (with the fraction of the measured HBM copy rate), TFLOP/s at 4096
+    (with the fraction of the measured bf16 burst rate)."""
     import torch
     import rank_weight_reconstruction_wl_gb300 as wl
     import wl_synth
@@ -802,15 +805,17 @@ def measure_large(dev, nsets=2):
             st.synchronize()
         return a0.elapsed_time(a1) / (reps * nsets) * 1e-3  # s
 
+    hbm_peak, tc_peak, kind = load_peaks()
     out = {"shapes": "hidden 5376, inter 21504, q/k/v 4096/2048/2048, r=64, bf16",
-           "l2": f"{nsets} weight sets rotated (1.56 GB, larger than L2)"}
+           "l2": f"{nsets} weight sets rotated ({0.78 * nsets:.2f} GB, larger than L2)",
+           "peaks": f"{hbm_peak} GB/s, {tc_peak} TFLOP/s bf16 burst ({kind})"}
     bf = dict(dtype=torch.bfloat16, device=dev)
-    for T in (1, 64, 4096):
+    for T in Ts:
         x = torch.randn(T, H, generator=g, device=dev).to(torch.bfloat16)
         yq, yk, yv = torch.empty(T, Q, **bf), torch.empty(T, KV, **bf), torch.empty(T, KV, **bf)
         ym = torch.empty(T, H, **bf)
         ws = wl.mlp_workspace(T, H, I, r, torch.bfloat16, dev)
-        reps = 10 if T < 4096 else 2
+        reps = reps_small if T < 4096 else 2
         tq = timeit(lambda w: wl.wl_qkv_fused(x, w["q"], w["k"], w["v"], outs=(yq, yk, yv), stream=st), reps)
         tm = timeit(lambda w: wl.wl_mlp_geglu_fused(x, w["gate"], w["up"], w["down"], y=ym, workspace=ws,
                                                     stream=st), reps)
@@ -819,12 +824,16 @@ def measure_large(dev, nsets=2):
             bm = (2 * (2 * I * H + 4 * I + 2 * r * (H + I)) + (2 * H * I + 4 * H + 2 * r * (I + H))
                   + 2 * T * 2 * H)
             out[f"T{T}"] = {"qkv_us": round(tq * 1e6, 1), "qkv_GBs": round(bq / tq / 1e9, 1),
-                            "mlp_us": round(tm * 1e6, 1), "mlp_GBs": round(bm / tm / 1e9, 1)}
+                            "qkv_frac": round(bq / tq / 1e9 / hbm_peak, 3),
+                            "mlp_us": round(tm * 1e6, 1), "mlp_GBs": round(bm / tm / 1e9, 1),
+                            "mlp_frac": round(bm / tm / 1e9 / hbm_peak, 3)}
         else:
             fq = 2 * T * (H * (Q + 2 * KV) + r * 3 * H + r * (Q + 2 * KV))
             fm = 2 * T * (3 * H * I + r * 3 * (H + I))
             out[f"T{T}"] = {"qkv_us": round(tq * 1e6, 1), "qkv_TFLOPs": round(fq / tq / 1e12, 1),
-                            "mlp_us": round(tm * 1e6, 1), "mlp_TFLOPs": round(fm / tm / 1e12, 1)}
+                            "qkv_frac": round(fq / tq / 1e12 / tc_peak, 3),
+                            "mlp_us": round(tm * 1e6, 1), "mlp_TFLOPs": round(fm / tm / 1e12, 1),
+                            "mlp_frac": round(fm / tm / 1e12 / tc_peak, 3)}
         del ws
     return out
 
@@ -857,6 +866,9 @@ def main():
                     help="stack kernel (one launch per 24 layers) or per-projection CUDA graph")
     ap.add_argument("--only-prefill", action="store_true",
                     help="run only the T=2048 prefill layer measurement (for profiling)")
+    ap.add_argument("--only", default=None, choices=["large1", "stack32", "materialize"],
+                    help="run one measurement alone, for profiling: the large set at one token "
+                         "(one weight set), a 4-layer stack at 32 tokens, or wl_materialize")
     ap.add_argument("--layers", type=int, default=L_LAYERS,
                     help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()
@@ -875,6 +887,20 @@ def main():
         dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
         torch.cuda.set_device(dev)
         print(json.dumps({"prefill_T2048": measure_prefill(dev, nlayers=min(args.layers, 4), reps=1)}))
+        return
+    if args.only:
+        import torch
+
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0")))
+        torch.cuda.set_device(dev)
+        if args.only == "large1":
+            res = measure_large(dev, nsets=1, Ts=(1,), reps_small=2)
+        elif args.only == "stack32":
+            res = measure_stack_grid(dev, steps=3, Ts=(32,), Gs=(L_LAYERS,), ranks=(args.rank,),
+                                     nlayers=min(args.layers, 4))
+        else:
+            res = measure_materialize(dev, r=args.rank, nsets=1, reps=2)
+        print(json.dumps({args.only: res}))
         return
     run_wl(args)
 

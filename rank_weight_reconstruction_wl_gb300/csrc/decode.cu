@@ -602,10 +602,8 @@ __global__ void __launch_bounds__(kDecThreads, 2) dec_linear_kernel(const __grid
     const float *sv_p = reinterpret_cast<const float *>(prefetch(sbuf, sg.s + r0, nrows * 4));
     const bf16 *Vp = sg.V + (int64_t)k0 * a.r;
     const bf16 *Up = sg.U + (int64_t)r0 * a.r;
-    if (a.r > 0 && a.vbuf > 0) {
-        if (!ZW) Vp = reinterpret_cast<const bf16 *>(prefetch(vbuf, Vp, klen * a.r * 2));
-        Up = reinterpret_cast<const bf16 *>(prefetch(ubuf, Up, nrows * a.r * 2));
-    }
+    if (a.r > 0 && a.vbuf > 0) Vp = reinterpret_cast<const bf16 *>(prefetch(vbuf, Vp, klen * a.r * 2));
+    if (a.r > 0 && a.ubuf > 0) Up = reinterpret_cast<const bf16 *>(prefetch(ubuf, Up, nrows * a.r * 2));
     pdl_wait();  // x comes from the previous kernel on the stream
     stage_x(a.x, a.in, a.T, k0, klen, ktiles * kBK, a.T, xb, a.xs32);
     consumer_sync();
@@ -1299,7 +1297,8 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
         const int xs = x_stride32(Kc);
         int pre = 0;
         const int vb = round_up(Kc * (int)r * 2 + 16, 16), ub = round_up(tpc * kBR * (int)r * 2 + 16, 16);
-        if (r > 0 && vb + ub <= kPrefetchBudget) pre = vb + ub;
+        if (r > 0 && zw && ub <= kPrefetchBudget) pre = ub;  // the z warps read V in place
+        else if (r > 0 && vb + ub <= kPrefetchBudget) pre = vb + ub;
         const int other = (int)T * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + cdiv(T, 8) * 8 * rp0 + 512) +
                           tpc * kBR * 4 + 16 + pre;
         const int nst = ring_stages(other, di);
@@ -1353,7 +1352,9 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
     const int rp = r > 0 ? (int)r : 1;
     // prefetch the V slice and U rows into shared memory when they are small
     const int vb = round_up(sp.Kc * (int)r * 2 + 16, 16), ub = round_up(sp.tpc * kBR * (int)r * 2 + 16, 16);
-    if (r > 0 && vb + ub <= kPrefetchBudget) {
+    if (r > 0 && zw && ub <= kPrefetchBudget) {
+        a.ubuf = ub;
+    } else if (r > 0 && vb + ub <= kPrefetchBudget) {
         a.vbuf = vb;
         a.ubuf = ub;
     }
