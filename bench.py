@@ -412,6 +412,7 @@ def run_wl(args):
         if not args.no_prefill:
             line["prefill_T2048"] = measure_prefill(dev)
             line["prefill_T2048_r32"] = measure_prefill(dev, r=32, reps=2)
+            line["matmul_yardstick_T2048"] = measure_matmul_yardstick(dev)
             line["large_set"] = measure_large(dev)
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = time_oracle_sample(r)
@@ -553,6 +554,44 @@ def measure_prefill(dev, T=2048, r=16, nlayers=4, reps=5):
             "layer_gflop": round(flops / 1e9, 2), "parts": out_parts,
             "timing": "CUDA graph replay of the layer's launches (device time)",
             "l2": f"{nlayers} weight sets rotated (larger than L2)"}
+
+
+def measure_matmul_yardstick(dev, T=2048, reps=20):
+    """A measurement only, not a hot-path option: torch.matmul (the vendor
+    library) in bf16 on the dense products of the prefill MLP at T tokens,
+    [T x 1152] x [1152 x 13824] (gate and up) and [T x 6912] x [6912 x 1152]
+    (down), over 4 weight sets (larger than L2).  Gives the rate a library GEMM
+    attains at these K, against which the weightless prefill kernel is read."""
+    import torch
+
+    h, i = SHAPES["hidden"], SHAPES["inter"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(23)
+    bf = dict(dtype=torch.bfloat16, device=dev)
+    out = {"timing": f"CUDA events over {reps} passes of 4 weight sets"}
+    _, bf16_peak, kind = load_peaks()
+    for name, K, N in (("gate_up", h, 2 * i), ("down", i, h)):
+        a = torch.randn(T, K, generator=g, device=dev).to(torch.bfloat16)
+        bs = [torch.randn(K, N, generator=g, device=dev).to(torch.bfloat16) for _ in range(4)]
+        c = torch.empty(T, N, **bf)
+        for b in bs:
+            torch.matmul(a, b, out=c)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            for b in bs:
+                torch.matmul(a, b, out=c)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / (reps * len(bs))
+        tf = 2 * T * K * N / (ms * 1e-3) / 1e12
+        out[name] = {"shape": f"[{T} x {K}] x [{K} x {N}]", "us": round(ms * 1e3, 2), "tflops": round(tf, 1),
+                     "frac_of_bf16_peak": round(tf / bf16_peak, 4)}
+        del a, bs, c
+    out["peak_kind"] = kind
+    return out
 
 
 def unique_bytes(shapes, L, G, T, r):

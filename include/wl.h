@@ -47,7 +47,9 @@ typedef enum {
     WL_ERR_UNSUPPORTED = 2, /* valid arguments this build cannot run       */
     WL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed        */
     WL_ERR_TIMEOUT = 4,     /* a bounded device-side wait gave up          */
-    WL_ERR_WORKSPACE = 5    /* workspace missing, misaligned or too small  */
+    WL_ERR_WORKSPACE = 5,   /* workspace missing, misaligned or too small  */
+    WL_ERR_INTERNAL = 6     /* a plan broke an invariant of the library;
+                               nothing was launched (a library bug)        */
 } wl_status;
 
 typedef enum { WL_OUT_BF16 = 0, WL_OUT_F32 = 1 } wl_out_dtype;

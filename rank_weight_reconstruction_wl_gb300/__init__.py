@@ -25,17 +25,17 @@ __all__ = [
     "wl_mlp_geglu_fused", "wl_mlp_geglu_fused_noalloc", "wl_materialize", "wl_decompose_band", "decompose",
     "wl_band_of_layer", "wl_device_status",
     "wl_last_error", "wl_version", "wl_selftest_wait", "WLStack", "EXPORTED_SYMBOLS", "WL_OK", "WL_ERR_INVALID_ARG",
-    "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_MAX_RANK",
+    "WL_ERR_UNSUPPORTED", "WL_ERR_CUDA", "WL_ERR_TIMEOUT", "WL_ERR_WORKSPACE", "WL_ERR_INTERNAL", "WL_MAX_RANK",
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libwl.so")
 
-WL_OK, WL_ERR_INVALID_ARG, WL_ERR_UNSUPPORTED, WL_ERR_CUDA, WL_ERR_TIMEOUT, WL_ERR_WORKSPACE = range(6)
+WL_OK, WL_ERR_INVALID_ARG, WL_ERR_UNSUPPORTED, WL_ERR_CUDA, WL_ERR_TIMEOUT, WL_ERR_WORKSPACE, WL_ERR_INTERNAL = range(7)
 WL_OUT_BF16, WL_OUT_F32 = 0, 1
 WL_MAX_RANK = 128
 STATUS_NAMES = {0: "WL_OK", 1: "WL_ERR_INVALID_ARG", 2: "WL_ERR_UNSUPPORTED", 3: "WL_ERR_CUDA",
-                4: "WL_ERR_TIMEOUT", 5: "WL_ERR_WORKSPACE"}
+                4: "WL_ERR_TIMEOUT", 5: "WL_ERR_WORKSPACE", 6: "WL_ERR_INTERNAL"}
 
 # Every function include/wl.h declares.
 EXPORTED_SYMBOLS = ("wl_linear", "wl_qkv_fused", "wl_linear_f32", "wl_qkv_fused_f32", "wl_decompose_workspace_bytes",

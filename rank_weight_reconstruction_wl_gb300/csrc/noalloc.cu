@@ -8,8 +8,6 @@
 // in a fixed, file-scope device array and exposes one more entry point that
 // uses it.  The array is part of the loaded module: every GPU that loads
 // libwl.so holds it until the process exits.
-#include <mutex>
-
 #include "wl_internal.cuh"
 
 namespace wl {
@@ -21,28 +19,17 @@ constexpr size_t kNoAllocScratchBytes = (size_t)4 << 20;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kNoAllocMaxDevices = 64;
-static void *g_scratch_addr[kNoAllocMaxDevices];
-static std::mutex g_scratch_mu;
-
-// Device address of g_noalloc_scratch on the current device.  The name
-// g_noalloc_scratch in host code is only a host-side stand-in, so the address
-// is looked up once per device, with that device current.
+// Device address of g_noalloc_scratch in the current context.  The name
+// g_noalloc_scratch in host code is only a host-side stand-in; the address is
+// looked up on every call (a few microseconds next to the launches), so a
+// device reset or a re-created primary context, which loads the module
+// again, never leaves a stale address behind.
 static wl_status scratch_address(void **out)
 {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= kNoAllocMaxDevices)
-        return fail(WL_ERR_UNSUPPORTED, "device index %d out of range", dev);
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(built-in scratch)");
+    *out = p;
     return WL_OK;
 }
 

@@ -64,6 +64,16 @@
 
 namespace wl {
 
+// Ring stages for `warps` consumer warps that take boxes round-robin: a
+// multiple of the warp count.  Box j of a phase goes to warp j % warps and to
+// stage (phase start + j) % nst, so every use of a stage within a phase falls
+// to one warp, in order.  Otherwise a warp could wait for a stage's next use
+// before the previous one (another warp's box) has landed, and a parity wait
+// cannot tell that phase from the one two uses back: it would return at once,
+// read the stage early and release it out of turn.  wl_stack_decode checks
+// the rule again before every launch.
+static inline int round_ring_to_warps(int nst, int warps) { return nst / warps * warps; }
+
 constexpr int kStThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
 constexpr int kStMaxT = 4;                 // tokens per launch
 constexpr int kStMaxR = 32;                // rank
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
             for (int i = 0; i < n; ++i) {
                 s = (s == 0 ? a.nst : s) - 1;
                 if (s == a.nst - 1) ph ^= 1u;
-                mbar_wait(&full[s], ph, a.status, kWaitRingFull);
+                if (!mbar_wait(&full[s], ph, a.status, kWaitRingFull)) atomicOr(a.status, kWaitDrain);
             }
         }
         return;
@@ -990,13 +1000,7 @@ extern "C" wl_status wl_stack_create(wl_stack *out, const wl_layer *layers, cons
     if (nst > 32) nst = 32;
     if (nst < kWarps)
         return fail(WL_ERR_UNSUPPORTED, "wl_stack_create: these shapes leave room for %d ring stages", nst);
-    // A multiple of the consumer warps: box j of a phase goes to warp j % 8 and
-    // to stage (phase start + j) % nst, so every use of a stage within a phase
-    // falls to one warp, in order.  Otherwise a warp could wait for a stage's
-    // next use before the previous one (another warp's box) has landed, and a
-    // parity wait cannot tell that phase from the one two uses back: it would
-    // return at once, read the stage early and release it out of turn.
-    nst = nst / kWarps * kWarps;
+    nst = round_ring_to_warps(nst, kWarps);
     pl.smem = fixed + nst * per_stage;
 
     // ---- device memory: maps, phases, np/slot0, partial words
@@ -1196,6 +1200,9 @@ extern "C" wl_status wl_stack_decode(wl_stack stk, const void *x, void *stream)
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     for (size_t ch = 0; ch < pl.chunks.size(); ++ch) {
+        if (pl.chunks[ch].nst <= 0 || pl.chunks[ch].nst % kWarps != 0)
+            return fail(WL_ERR_INTERNAL, "wl_stack_decode: ring of %d stages is not a multiple of the %d "
+                        "consumer warps", pl.chunks[ch].nst, kWarps);
         StArgs a = pl.chunks[ch];  // a copy: calls on other threads may launch at the same time
         a.epoch = epoch;
         a.x = pl.chunk_x[ch] ? pl.chunk_x[ch] : static_cast<const bf16 *>(x);

@@ -27,8 +27,8 @@ def _tokens(T, n, seed):
 
 @pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (64, torch.float32), (4096, torch.bfloat16)])
 def test_large_qkv(wl, orc, gpu, T, ydt):
-    """T = 1 and 64 run the HBM-streaming kernel (64 tokens with a smaller
-    work split so that it fits in shared memory), T = 4096 the tensor cores."""
+    """T = 1 runs the HBM-streaming decode kernel (calls of up to 8 tokens
+    take it); T = 64 and 4096 run the tcgen05 tensor-core kernel."""
     x, ths = _qkv_case(500 + T, T)
     ys = wl.wl_qkv_fused(x.to(gpu), *[t.to(gpu) for t in ths], ydt=ydt)
     torch.cuda.synchronize()

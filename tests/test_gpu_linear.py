@@ -1,8 +1,13 @@
 """GPU parity of wl_linear and wl_qkv_fused against the fp64 oracle.
 
-The CUDA path and the oracle see the same seeded inputs (wl_synth).  Bar:
-max|y_gpu - y_ref| <= 1e-2 rms(y_ref) for bf16 outputs (y_ref after the final
-cast) and <= 1e-4 rms(y_ref) for fp32 outputs.
+The CUDA path and the oracle see the same seeded inputs (wl_synth).  Bar,
+against the exact fp64 result y_ref: max|y_gpu - y_ref| <= 1e-4 rms(y_ref) for
+fp32 outputs; for bf16 outputs the distance from y_ref to the set of values
+that round to y_gpu, max(0, |y_gpu - y_ref| - ulp(y_gpu)/2), <= 1e-2 rms(y_ref)
+(tests/parity.py, err_ratio).  Calls of up to 8 tokens run the HBM-streaming
+decode kernels (mma.sync), longer ones the tcgen05 tensor-core kernel: the
+measured crossover, below the 64 tokens the method's description allows the
+streaming form.
 """
 import numpy as np
 import pytest

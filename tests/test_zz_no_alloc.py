@@ -55,6 +55,44 @@ def test_noalloc_matches_workspace_entry_point(wl, gpu, ydt, code, T, r):
         assert err <= TOL[ydt] * rms, err
 
 
+@pytest.mark.parametrize("ydt,code", [(torch.bfloat16, 0), (torch.float32, 1)])
+@pytest.mark.parametrize("T", [16, 48])
+def test_noalloc_many_tokens_after_a_decode_call(wl, gpu, ydt, code, T):
+    """T > 8 takes the tensor-core MLP, whose workspace (fp32 g and u, then
+    the bf16 hi and lo parts of h) is laid out differently from the decode
+    path's; a decode-shape call first leaves its own data in the scratch.
+    48 tokens is close to the largest T the 4 MiB scratch holds for these
+    shapes with fp32 outputs."""
+    r = 16
+    xd, thd = _case(70, 1, 1152, 6912, r)
+    yd = torch.empty(1, 1152, dtype=ydt, device=gpu)
+    assert _call_noalloc(wl, xd.to(gpu), [t.to(gpu) for t in thd], yd, code, r) == wl.WL_OK
+    x, ths = _case(80 + T, T, 1152, 6912, r)
+    xg = x.to(gpu)
+    tg = [t.to(gpu) for t in ths]
+    ref = wl.wl_mlp_geglu_fused(xg, *tg, ydt=ydt).float()
+    rms = ref.pow(2).mean().sqrt().item()
+    y = torch.full((T, 1152), float("nan"), dtype=ydt, device=gpu)
+    st = _call_noalloc(wl, xg, tg, y, code, r)
+    assert st == wl.WL_OK, wl.wl_last_error()
+    assert wl.wl_device_status() == wl.WL_OK
+    err = (y.float() - ref).abs().max().item()
+    assert err <= TOL[ydt] * rms, err
+
+
+def test_noalloc_python_wrapper(wl, gpu):
+    x, ths = _case(5, 2, 1152, 6912, 4)
+    xg = x.to(gpu)
+    tg = [t.to(gpu) for t in ths]
+    ref = wl.wl_mlp_geglu_fused(xg, *tg).float()
+    y = torch.full((2, 1152), float("nan"), dtype=torch.bfloat16, device=gpu)
+    out = wl.wl_mlp_geglu_fused_noalloc(xg, *tg, y=y)
+    assert out is y
+    torch.cuda.synchronize()
+    rms = ref.pow(2).mean().sqrt().item()
+    assert (y.float() - ref).abs().max().item() <= TOL[torch.bfloat16] * rms
+
+
 def test_noalloc_rejects_sizes_beyond_scratch(wl, gpu):
     hidden, inter, r = 5376, 21504 * 8, 128
     need = wl.wl_mlp_workspace_bytes(1, hidden, inter, r)
