@@ -232,13 +232,16 @@ __device__ __forceinline__ void flush_piece(float *wb, int zoff, const float (&c
 }
 
 // Sums of partial words for NQ groups of 4 rows (i0 ..) of token t and NS
-// parts of a row tile of phase Q (n partials from slot0): every load of every
-// slot is issued before the epochs are checked, so a ready input costs one
-// round trip.  Sums run in slot order.  false: gave up (status set).
+// parts of a row tile of phase Q (n partials from slot0).  The loads of up to
+// CH slots are issued before any of them is used, and the epochs are checked
+// without branching, so a ready input costs one L2 round trip per CH slots
+// rather than one per slot pair (the poll sits on the path between phases).
+// Sums run in slot order.  false: gave up (status set).
 template <int NQ, int NS>
 __device__ __forceinline__ bool sumq(const StPhase &Q, int n, int slot0, int t, int i0, int T, unsigned epoch,
                                      float (&out)[NS][NQ * 4], unsigned *status)
 {
+    constexpr int CH = 4 / (NQ * NS) > 0 ? 4 / (NQ * NS) : 1;  // slots in flight: 8 loads of 16 bytes
     const size_t stride = (size_t)Q.nsub * T * kStBox;
     const unsigned long long *base = Q.part + (size_t)slot0 * Q.nsub * T * kStBox + t * kStBox + i0;
     long long t0 = -1;
@@ -248,23 +251,39 @@ __device__ __forceinline__ bool sumq(const StPhase &Q, int n, int slot0, int t, 
         for (int ps = 0; ps < NS; ++ps)
 #pragma unroll
             for (int e = 0; e < NQ * 4; ++e) acc[ps][e] = 0.f;
-        bool ok = true;
-#pragma unroll 2
-        for (int j = 0; j < n; ++j) {
+        unsigned bad = 0;
+        for (int j0 = 0; j0 < n; j0 += CH) {
+            ulonglong2 w[CH][NS][NQ][2];
 #pragma unroll
-            for (int ps = 0; ps < NS; ++ps)
+            for (int jj = 0; jj < CH; ++jj)
 #pragma unroll
-                for (int q = 0; q < NQ; ++q) {
-                    const unsigned long long *pp = base + j * stride + (size_t)ps * T * kStBox + 4 * q;
-                    const ulonglong2 u = ld_words2(pp), v = ld_words2(pp + 2);
-                    ok = ok && word_ok(u.x, epoch) && word_ok(u.y, epoch) && word_ok(v.x, epoch) && word_ok(v.y, epoch);
-                    acc[ps][4 * q] += word_val(u.x);
-                    acc[ps][4 * q + 1] += word_val(u.y);
-                    acc[ps][4 * q + 2] += word_val(v.x);
-                    acc[ps][4 * q + 3] += word_val(v.y);
-                }
+                for (int ps = 0; ps < NS; ++ps)
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        if (j0 + jj < n) {
+                            const unsigned long long *pp = base + (j0 + jj) * stride + (size_t)ps * T * kStBox + 4 * q;
+                            w[jj][ps][q][0] = ld_words2(pp);
+                            w[jj][ps][q][1] = ld_words2(pp + 2);
+                        }
+                    }
+#pragma unroll
+            for (int jj = 0; jj < CH; ++jj) {
+                if (j0 + jj < n)
+#pragma unroll
+                for (int ps = 0; ps < NS; ++ps)
+#pragma unroll
+                    for (int q = 0; q < NQ; ++q) {
+                        const ulonglong2 u = w[jj][ps][q][0], v = w[jj][ps][q][1];
+                        bad |= ((unsigned)(u.x >> 32) ^ epoch) | ((unsigned)(u.y >> 32) ^ epoch) |
+                               ((unsigned)(v.x >> 32) ^ epoch) | ((unsigned)(v.y >> 32) ^ epoch);
+                        acc[ps][4 * q] += word_val(u.x);
+                        acc[ps][4 * q + 1] += word_val(u.y);
+                        acc[ps][4 * q + 2] += word_val(v.x);
+                        acc[ps][4 * q + 3] += word_val(v.y);
+                    }
+            }
         }
-        if (ok) {
+        if (!bad) {
 #pragma unroll
             for (int ps = 0; ps < NS; ++ps)
 #pragma unroll

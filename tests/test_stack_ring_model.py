@@ -85,3 +85,4 @@ def test_host_rounding_matches_rule():
         for n in range(W, 64):
             r = round_ring_to_warps(n, W)
             assert r % W == 0 and r <= n and n - r < W
+
