@@ -40,14 +40,17 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
     const int i0 = i_base + tc * 8;
     const bool col_ok = i0 < in;      // in % 8 == 0: a chunk of 8 columns is all in or all out
 
-    // the thread's W0 chunks first: their HBM round trip overlaps the staging
-    // of U and V and the rank-r products
+    // the thread's W0 chunks and row scales first: their round trips overlap
+    // the staging of U and V and the rank-r products (loaded later, inside the
+    // row loop with its early exit, the scales would cost one round trip per row)
     uint4 wv[8];
+    float sv[8];
 #pragma unroll
     for (int a = 0; a < 8; ++a) {
         const int o = o_base + tr * 8 + a;
-        wv[a] = (col_ok && o < out) ? *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0)
-                                    : make_uint4(0u, 0u, 0u, 0u);
+        const bool ok = col_ok && o < out;
+        wv[a] = ok ? *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0) : make_uint4(0u, 0u, 0u, 0u);
+        sv[a] = ok ? s[o] : 0.f;
     }
 
     float d[8][8];
@@ -90,13 +93,12 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
     for (int a = 0; a < 8; ++a) {
         const int o = o_base + tr * 8 + a;
         if (o >= out) break;
-        const float sv = s[o];
         const float w0[8] = {bf_lo(wv[a].x), bf_hi(wv[a].x), bf_lo(wv[a].y), bf_hi(wv[a].y),
                              bf_lo(wv[a].z), bf_hi(wv[a].z), bf_lo(wv[a].w), bf_hi(wv[a].w)};
         float w[8];
 #pragma unroll
         for (int b = 0; b < 8; ++b) {
-            w[b] = __fmul_rn(sv, w0[b]);
+            w[b] = __fmul_rn(sv[a], w0[b]);
             if (r > 0) w[b] = __fadd_rn(w[b], d[a][b]);
         }
         if (F32OUT) {
