@@ -238,6 +238,14 @@ __device__ __forceinline__ bool ring_wait_empty(uint64_t *bar, unsigned parity, 
 
 // A 2D tile copy addressed by a shared-memory offset (no address conversion
 // per copy).
+// Prefetch of a 2D box of `map` into L2 (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap *map, int c0, int c1)
+{
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1)
+                 : "memory");
+}
 __device__ __forceinline__ void tma_load_2d_u32(uint32_t dst, const CUtensorMap *map, int c0, int c1, uint64_t *bar)
 {
     asm volatile(

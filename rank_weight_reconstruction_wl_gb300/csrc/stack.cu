@@ -448,6 +448,24 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 const uint32_t sdst = w_base + (uint32_t)s * (uint32_t)sbytes_stage;
                 tma_load_2d_u32(sdst, m, kb * kStBox, row0, fb);
                 if (a.rpad) tma_load_2d_u32(sdst + kStBoxBytes, vm, kb * kStBox, 0, fb);
+                // the box one ring ahead in this phase, into L2: when the
+                // ring is full at the phase's start, its refill then comes
+                // from L2 instead of HBM
+                if (b + a.nst < b1) {
+                    const int bq = b + a.nst, rtq = bq / bpr, wq = bq - rtq * bpr;
+                    int sq, kq, rq;
+                    if (gu) {
+                        sq = wq >= KB ? 1 : 0;
+                        kq = wq - sq * KB;
+                        rq = rtq * kStBox;
+                    } else {
+                        sq = rtq >= rt0[2] ? 2 : (rtq >= rt0[1] ? 1 : 0);
+                        kq = wq;
+                        rq = (rtq - (sq == 2 ? rt0[2] : sq == 1 ? rt0[1] : 0)) * kStBox;
+                    }
+                    tma_prefetch_2d(sq == 2 ? map[2] : sq == 1 ? map[1] : map[0], kq * kStBox, rq);
+                    if (a.rpad) tma_prefetch_2d(sq == 2 ? vtm[2] : sq == 1 ? vtm[1] : vtm[0], kq * kStBox, 0);
+                }
                 ++issued;
                 if (++s == a.nst) {
                     s = 0;
