@@ -9,25 +9,28 @@
 // and, for a bf16 result, one round-to-nearest-even.  The tensor cores are
 // not used: their accumulation order is not this one.
 //
-// Tiling: a CTA owns a 64 x 256 tile of W_eff (8 rows x 8 columns per
-// thread).  Each thread loads its W0 chunks before anything else, so that
+// Tiling: a CTA owns a 32 x 256 tile of W_eff (4 rows x 8 columns per
+// thread, 80 registers, three CTAs per SM: with 64-row tiles and 127 registers
+// only two fit, and an SM's HBM requests stall between one CTA's loads and the
+// next's).  Each thread loads its W0 chunks before anything else, so that
 // their HBM round trip overlaps the rank-r work.  U and V are staged through
 // shared memory in chunks of 32 ranks (read row-major, coalesced; stored
 // transposed, so each k step reads one float4 pair of V and of U), which keeps
 // the rank-r operands out of HBM after their first read: V is re-read once
-// per 64 output rows, U once per 256 input columns, both from L2.
+// per 32 output rows, U once per 256 input columns, both from L2.
 #include "wl_internal.cuh"
 
 namespace wl {
 
-constexpr int kMatRows = 64;
+constexpr int kMatRowsPerThread = 4;
+constexpr int kMatRows = 8 * kMatRowsPerThread;  // tile rows: 8 row groups of the thread's rows
 constexpr int kMatCols = 256;
 constexpr int kMatK = 32;
 constexpr int kUStr = kMatRows + 4;  // padded row strides (floats), multiples of 4
 constexpr int kVStr = kMatCols + 4;
 
 template <int F32OUT>
-__global__ void __launch_bounds__(kThreads) materialize_kernel(
+__global__ void __launch_bounds__(kThreads, 3) materialize_kernel(
     const bf16 *__restrict__ W0, const float *__restrict__ s, const bf16 *__restrict__ U,
     const bf16 *__restrict__ V, void *__restrict__ Weff, int out, int in, int r)
 {
@@ -35,7 +38,7 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
     __shared__ __align__(16) float Vs[kMatK * kVStr];
     const int o_base = blockIdx.y * kMatRows;
     const int i_base = blockIdx.x * kMatCols;
-    const int tr = threadIdx.x >> 5;  // rows o_base + tr*8 .. +7
+    const int tr = threadIdx.x >> 5;  // rows o_base + tr*RPT .. +RPT-1
     const int tc = threadIdx.x & 31;  // cols i_base + tc*8 .. +7
     const int i0 = i_base + tc * 8;
     const bool col_ok = i0 < in;      // in % 8 == 0: a chunk of 8 columns is all in or all out
@@ -43,19 +46,20 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
     // the thread's W0 chunks and row scales first: their round trips overlap
     // the staging of U and V and the rank-r products (loaded later, inside the
     // row loop with its early exit, the scales would cost one round trip per row)
-    uint4 wv[8];
-    float sv[8];
+    constexpr int RPT = kMatRowsPerThread;
+    uint4 wv[RPT];
+    float sv[RPT];
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int o = o_base + tr * 8 + a;
+    for (int a = 0; a < RPT; ++a) {
+        const int o = o_base + tr * RPT + a;
         const bool ok = col_ok && o < out;
         wv[a] = ok ? *reinterpret_cast<const uint4 *>(W0 + (int64_t)o * in + i0) : make_uint4(0u, 0u, 0u, 0u);
         sv[a] = ok ? s[o] : 0.f;
     }
 
-    float d[8][8];
+    float d[RPT][8];
 #pragma unroll
-    for (int a = 0; a < 8; ++a)
+    for (int a = 0; a < RPT; ++a)
 #pragma unroll
         for (int b = 0; b < 8; ++b) d[a][b] = 0.0f;
 
@@ -74,14 +78,13 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
         }
         __syncthreads();
         for (int k = 0; k < kn; ++k) {
-            const float4 u0 = *reinterpret_cast<const float4 *>(Us + k * kUStr + tr * 8);
-            const float4 u1 = *reinterpret_cast<const float4 *>(Us + k * kUStr + tr * 8 + 4);
+            const float4 u0 = *reinterpret_cast<const float4 *>(Us + k * kUStr + tr * RPT);
             const float4 v0 = *reinterpret_cast<const float4 *>(Vs + k * kVStr + tc * 8);
             const float4 v1 = *reinterpret_cast<const float4 *>(Vs + k * kVStr + tc * 8 + 4);
-            const float uu[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+            const float uu[4] = {u0.x, u0.y, u0.z, u0.w};
             const float vv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < RPT; ++a)
 #pragma unroll
                 for (int b = 0; b < 8; ++b) d[a][b] = __fmaf_rn(uu[a], vv[b], d[a][b]);
         }
@@ -90,8 +93,8 @@ __global__ void __launch_bounds__(kThreads) materialize_kernel(
 
     if (!col_ok) return;
 #pragma unroll
-    for (int a = 0; a < 8; ++a) {
-        const int o = o_base + tr * 8 + a;
+    for (int a = 0; a < RPT; ++a) {
+        const int o = o_base + tr * RPT + a;
         if (o >= out) break;
         const float w0[8] = {bf_lo(wv[a].x), bf_hi(wv[a].x), bf_lo(wv[a].y), bf_hi(wv[a].y),
                              bf_lo(wv[a].z), bf_hi(wv[a].z), bf_lo(wv[a].w), bf_hi(wv[a].w)};
