@@ -93,8 +93,10 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
 /*
  * wl_mlp_workspace_bytes -- bytes of device workspace wl_mlp_geglu_fused
  * needs for these sizes (the intermediate h = gelu(g)*u and the partial sums
- * of the down projection's low-rank input h V_down).  Returns 0 for invalid
- * sizes.
+ * of the down projection's low-rank input h V_down).  Calls of up to 8 tokens
+ * run the HBM-streaming kernels unless no launch plan of theirs fits shared
+ * memory for these sizes (then the tensor-core kernels run); the size covers
+ * both.  Returns 0 for invalid sizes.
  */
 size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t r,
                               wl_out_dtype ydt);

@@ -1204,7 +1204,7 @@ static int cluster_capacity(const void *fn, int ks, int smem, const DeviceInfo *
 //     formed by four separate warps during the stream (zw) it runs at about
 //     12 GB/s and costs only what the stream does not hide;
 //   * clusters of 5, 7 or 8 CTAs place unevenly on the GPCs and measured far
-//     slower than this predicts; they are not used.
+//     slower than this predicts; they are used only where no other size fits.
 constexpr double kHbmBytesPerUs = 6.8e6;
 constexpr double kStageLatUs = 2.34;
 constexpr double kZBytesPerUs = 4.0e4;    // x V after the stream, 8 warps
@@ -1224,11 +1224,13 @@ static bool plan_balanced(const int *seg_tiles, int nseg, int in, int r, int pai
     int best_ctas = 0;
     bool found = false;
     const int S = di->sm_count;
+    // the preferred cluster sizes first; 5, 7 and 8 only where nothing else fits
+    for (int pass = 0; pass < 2 && !found; ++pass)
     for (int tpc = 1; tpc <= tpc_max; ++tpc) {
         int ngrp = 0;
         for (int j = 0; j < nseg; ++j) ngrp += cdiv(seg_tiles[j], tpc);
-        for (int ks = 1; ks <= 6; ++ks) {
-            if (ks == 5) continue;
+        for (int ks = 1; ks <= 8; ++ks) {
+            if ((ks == 5 || ks > 6) != (pass == 1)) continue;
             const int Kc = round_up(cdiv(in, ks), kBK);
             if (Kc > max_kc || cdiv(in, Kc) != ks) continue;
             const int ctas = ngrp * ks;
@@ -1271,9 +1273,11 @@ static wl_status w0_map(const void *W0, int64_t K, int64_t out, CUtensorMap *m, 
     return tmap_2d_bf16(W0, K, out, K, kBK, kBR, m);
 }
 
+// plan_only: find (and cache) the launch plan, launch nothing; WL_ERR_UNSUPPORTED
+// when no plan fits shared memory.
 static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, void *const *y,
                                  int64_t T, int64_t in, int64_t r, int ydt, cudaStream_t st,
-                                 const DeviceInfo *di)
+                                 const DeviceInfo *di, bool plan_only = false)
 {
     wl_status s = WL_OK;
     const int NT = nt_round(cdiv(T, 8));
@@ -1323,6 +1327,7 @@ static wl_status dec_linear_once(const bf16 *x, const wl_proj *proj, int nproj, 
         }
     }
 
+    if (plan_only) return WL_OK;
     DecArgs a = {};
     a.x = x;
     a.T = (int)T;
@@ -1390,6 +1395,18 @@ wl_status launch_decode_linear(const bf16 *x, const wl_proj *proj, int nproj, vo
     return WL_OK;
 }
 
+bool decode_linear_fits(const wl_proj *proj, int nproj, int64_t T, int64_t in, int64_t r, int ydt)
+{
+    wl_status s = WL_OK;
+    const DeviceInfo *di = device_info(&s);
+    if (!di) return false;
+    const int64_t Tc = T < kDecodeMaxT ? T : kDecodeMaxT;
+    void *ys[3] = {};
+    const bool ok = dec_linear_once(nullptr, proj, nproj, ys, Tc, in, r, ydt, nullptr, di, true) == WL_OK;
+    clear_error();
+    return ok;
+}
+
 // ---- MLP ---------------------------------------------------------------
 size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r)
 {
@@ -1399,13 +1416,14 @@ size_t decode_mlp_workspace_bytes(int64_t hidden, int64_t inter, int64_t r)
     return (size_t)(256 + al(kTokChunk * inter * 4) + al((int64_t)kMaxPartials * kTokChunk * rp * 4));
 }
 
+// Both launches are planned before either is made; plan_only: find (and cache)
+// the plans, launch nothing; WL_ERR_UNSUPPORTED when one does not fit.
 static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj &up,
                               const wl_proj &down, void *y, int T, int hidden, int inter, int r,
-                              char *ws, int ydt, cudaStream_t st, const DeviceInfo *di)
+                              char *ws, int ydt, cudaStream_t st, const DeviceInfo *di,
+                              bool plan_only = false)
 {
     const int rp = r > 0 ? r : 1;
-    float *h = reinterpret_cast<float *>(ws + 256);
-    float *zd = reinterpret_cast<float *>(ws + 256 + ((int64_t)kTokChunk * inter * 4 + 255) / 256 * 256);
 
     // launch 1: gate and up tiles, h, partials of h V_down
     GateUpArgs g = {};
@@ -1444,6 +1462,39 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
             g_plans[key] = sg;
         }
     }
+    // launch 2: down tiles, input h as bf16 hi/lo columns
+    DownArgs d = {};
+    const int NT = nt_round(cdiv(2 * T, 8));
+    const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
+    s = ensure_attrs((const void *)dfn, 0, di);
+    if (s != WL_OK) return s;
+    auto dsmem_of = [&](int tpc, int Kc, int *nst_out) {
+        const int xs = x_stride32(Kc);
+        const int ub = round_up(tpc * kBR * r * 2 + 16, 16);
+        const int pre = (r > 0 && ub <= kPrefetchBudget) ? ub : 0;
+        const int other = 2 * T * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) + tpc * kBR * 4 + 16 + pre;
+        const int nst = ring_stages(other, di);
+        *nst_out = nst;
+        return nst < 2 ? -1 : carve_head_bytes(nst) + other;
+    };
+    Split sd;
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        const uint64_t key = plan_key(3, di->device, hidden, inter, r, T);
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            sd = it->second;
+        } else {
+            const int dt = cdiv(hidden, kBR);
+            if (!plan_balanced(&dt, 1, inter, r, 1, 0, false, (48 * 1024) / (2 * T * 2) / kBK * kBK, 8, 1 << 20,
+                               (const void *)dfn, dsmem_of, di, &sd))
+                return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
+            g_plans[key] = sd;
+        }
+    }
+    if (plan_only) return WL_OK;  // both launches have a plan
+    float *h = reinterpret_cast<float *>(ws + 256);
+    float *zd = reinterpret_cast<float *>(ws + 256 + ((int64_t)kTokChunk * inter * 4 + 255) / 256 * 256);
     s = w0_map(gate.W0, hidden, inter, &g.mapg, &g.blk);
     if (s != WL_OK) return s;
     s = w0_map(up.W0, hidden, inter, &g.mapu, &g.blk);
@@ -1488,36 +1539,6 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     s = launch((const void *)gfn, sg.ngrp * sg.KS, sg.KS, gsmem, st, gargs);
     if (s != WL_OK) return s;
 
-    // launch 2: down tiles, input h as bf16 hi/lo columns
-    DownArgs d = {};
-    const int NT = nt_round(cdiv(2 * T, 8));
-    const dn_fn dfn = g_dn[T == 1 ? 0 : 1][NT <= 1 ? 0 : 1];
-    s = ensure_attrs((const void *)dfn, 0, di);
-    if (s != WL_OK) return s;
-    auto dsmem_of = [&](int tpc, int Kc, int *nst_out) {
-        const int xs = x_stride32(Kc);
-        const int ub = round_up(tpc * kBR * r * 2 + 16, 16);
-        const int pre = (r > 0 && ub <= kPrefetchBudget) ? ub : 0;
-        const int other = 2 * T * xs * 4 + 4 * (tpc * kBR * 8 * NT + 512 * NT + 8 * rp + kThreads) + tpc * kBR * 4 + 16 + pre;
-        const int nst = ring_stages(other, di);
-        *nst_out = nst;
-        return nst < 2 ? -1 : carve_head_bytes(nst) + other;
-    };
-    Split sd;
-    {
-        std::lock_guard<std::mutex> lk(g_plan_mu);
-        const uint64_t key = plan_key(3, di->device, hidden, inter, r, T);
-        auto it = g_plans.find(key);
-        if (it != g_plans.end()) {
-            sd = it->second;
-        } else {
-            const int dt = cdiv(hidden, kBR);
-            if (!plan_balanced(&dt, 1, inter, r, 1, 0, false, (48 * 1024) / (2 * T * 2) / kBK * kBK, 8, 1 << 20,
-                               (const void *)dfn, dsmem_of, di, &sd))
-                return fail(WL_ERR_UNSUPPORTED, "MLP decode: shapes too large for shared memory");
-            g_plans[key] = sd;
-        }
-    }
     s = w0_map(down.W0, inter, hidden, &d.mapd, &d.blk);
     if (s != WL_OK) return s;
     d.h = h;
@@ -1549,6 +1570,19 @@ static wl_status dec_mlp_once(const bf16 *x, const wl_proj &gate, const wl_proj 
     if (s != WL_OK) return s;
     void *dargs[] = {&d};
     return launch((const void *)dfn, sd.ngrp * sd.KS, sd.KS, dsmem, st, dargs);
+}
+
+bool decode_mlp_fits(const wl_proj &gate, const wl_proj &up, const wl_proj &down, int64_t T, int64_t hidden,
+                     int64_t inter, int64_t r, int ydt)
+{
+    wl_status s = WL_OK;
+    const DeviceInfo *di = device_info(&s);
+    if (!di) return false;
+    const int Tc = (int)(T < kTokChunk ? T : kTokChunk);
+    const bool ok = dec_mlp_once(nullptr, gate, up, down, nullptr, Tc, (int)hidden, (int)inter, (int)r, nullptr,
+                                 ydt, nullptr, di, true) == WL_OK;
+    clear_error();
+    return ok;
 }
 
 wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up,

@@ -19,6 +19,8 @@ __device__ unsigned g_status_word;
 
 static thread_local char t_err[512];
 
+void clear_error() { t_err[0] = '\0'; }
+
 wl_status fail(wl_status st, const char *fmt, ...)
 {
     va_list ap;
@@ -157,7 +159,7 @@ wl_status wl_linear(const void *x, const void *W0, const float *s, const void *U
     WL_TRY(begin());
     wl_proj p = {W0, s, U, V, out};
     void *ys[1] = {y};
-    if (T > kDecodeMaxTokens)
+    if (T > kDecodeMaxTokens || !decode_linear_fits(&p, 1, T, in, r, ydt))
         return launch_prefill(static_cast<const bf16 *>(x), &p, 1, ys, T, in, in, in, r, ydt,
                               static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), &p, 1, ys, T, in, r, ydt,
@@ -177,7 +179,7 @@ wl_status wl_qkv_fused(const void *x, wl_proj q, wl_proj k, wl_proj v, void *yq,
         WL_TRY(check_theta(names[j], ps[j].W0, ps[j].s, ps[j].U, ps[j].V, r));
     }
     WL_TRY(begin());
-    if (T > kDecodeMaxTokens)
+    if (T > kDecodeMaxTokens || !decode_linear_fits(ps, 3, T, in, r, ydt))
         return launch_prefill(static_cast<const bf16 *>(x), ps, 3, ys, T, in, in, in, r, ydt,
                               static_cast<cudaStream_t>(stream));
     return launch_decode_linear(static_cast<const bf16 *>(x), ps, 3, ys, T, in, r, ydt,
@@ -229,8 +231,9 @@ size_t wl_mlp_workspace_bytes(int64_t T, int64_t hidden, int64_t inter, int64_t 
     if (T < 1 || hidden < 8 || inter < 8 || hidden % 8 || inter % 8 || r < 0 || r > WL_MAX_RANK ||
         hidden > kMaxDim || inter > kMaxDim || T > kMaxDim)
         return 0;
+    // few tokens run the decode kernels unless they have no plan for these
+    // shapes; the workspace covers both paths
     const size_t dec = decode_mlp_workspace_bytes(hidden, inter, r);
-    if (T <= kMlpDecodeMaxTokens) return dec;
     const size_t pre = prefill_mlp_workspace_bytes(T, inter, ydt);
     return pre > dec ? pre : dec;
 }
@@ -256,7 +259,7 @@ wl_status wl_mlp_geglu_fused(const void *x, wl_proj gate, wl_proj up, wl_proj do
     if (ws_bytes < need)
         return fail(WL_ERR_WORKSPACE, "workspace too small: %zu bytes, need %zu", ws_bytes, need);
     WL_TRY(begin());
-    if (T > kMlpDecodeMaxTokens)
+    if (T > kMlpDecodeMaxTokens || !decode_mlp_fits(gate, up, down, T, hidden, inter, r, ydt))
         return launch_prefill_mlp(static_cast<const bf16 *>(x), gate, up, down, y, T, hidden, inter, r,
                                   workspace, ws_bytes, ydt, static_cast<cudaStream_t>(stream));
     return launch_decode_mlp(static_cast<const bf16 *>(x), gate, up, down, y, T, hidden, inter, r,

@@ -86,12 +86,18 @@ wl_status tmap_kblocks_bf16(const void *base, int64_t K, int64_t rows, int box_r
 
 // Record a message for wl_last_error() and return the status.
 wl_status fail(wl_status st, const char *fmt, ...);
+void clear_error();  // empties this thread's message (after a probe that may fail)
 wl_status cuda_fail(cudaError_t e, const char *what);
 
 // Kernel launchers (arguments already validated by the C-ABI layer).
 wl_status launch_decode_linear(const bf16 *x, const wl_proj *proj, int nproj,
                                void *const *y, int64_t T, int64_t in, int64_t r,
                                int ydt, cudaStream_t st);
+// Whether the decode kernels have a launch plan for these shapes (shared
+// memory); where not, calls of few tokens take the tensor-core path.
+bool decode_linear_fits(const wl_proj *proj, int nproj, int64_t T, int64_t in, int64_t r, int ydt);
+bool decode_mlp_fits(const wl_proj &gate, const wl_proj &up, const wl_proj &down, int64_t T, int64_t hidden,
+                     int64_t inter, int64_t r, int ydt);
 wl_status launch_decode_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &up,
                             const wl_proj &down, void *y, int64_t T, int64_t hidden,
                             int64_t inter, int64_t r, void *ws, size_t ws_bytes,

@@ -25,7 +25,8 @@ def _tokens(T, n, seed):
     return np.sort(np.random.default_rng(seed).choice(T, n, replace=False))
 
 
-@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (64, torch.float32), (4096, torch.bfloat16)])
+@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (8, torch.bfloat16), (64, torch.float32),
+                                   (4096, torch.bfloat16)])
 def test_large_qkv(wl, orc, gpu, T, ydt):
     """T = 1 runs the HBM-streaming decode kernel (calls of up to 8 tokens
     take it); T = 64 and 4096 run the tcgen05 tensor-core kernel."""
@@ -39,8 +40,12 @@ def test_large_qkv(wl, orc, gpu, T, ydt):
         assert_parity(y[torch.as_tensor(tok, device=gpu)], ref, ydt, f"T={T} {name}")
 
 
-@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (64, torch.bfloat16), (4096, torch.bfloat16)])
+@pytest.mark.parametrize("T,ydt", [(1, torch.bfloat16), (4, torch.bfloat16), (8, torch.float32), (64, torch.bfloat16),
+                                   (4096, torch.bfloat16)])
 def test_large_mlp(wl, orc, gpu, T, ydt):
+    """T = 4: the decode kernels with an 8-CTA K split of the 21504-long down
+    projection (no smaller split fits the staged input); T = 8: no decode plan
+    fits, so the call runs the tcgen05 kernels."""
     g = wl_synth.make_generator(900 + T)
     x = wl_synth.draw_x(g, T, H)
     ths = [wl_synth.draw_theta(g, H, I, R), wl_synth.draw_theta(g, H, I, R), wl_synth.draw_theta(g, I, H, R)]
