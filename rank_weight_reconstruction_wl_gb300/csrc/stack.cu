@@ -450,8 +450,10 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 if (a.rpad) tma_load_2d_u32(sdst + kStBoxBytes, vm, kb * kStBox, 0, fb);
                 // the box one ring ahead in this phase, into L2: when the
                 // ring is full at the phase's start, its refill then comes
-                // from L2 instead of HBM
-                if (b + a.nst < b1) {
+                // from L2 instead of HBM.  Only W0, and only with a ring of 16
+                // stages or more: with a short ring (large ranks) the extra
+                // copies cost the producer more than they save.
+                if (a.nst >= 16 && b + a.nst < b1) {
                     const int bq = b + a.nst, rtq = bq / bpr, wq = bq - rtq * bpr;
                     int sq, kq, rq;
                     if (gu) {
@@ -464,7 +466,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                         rq = (rtq - (sq == 2 ? rt0[2] : sq == 1 ? rt0[1] : 0)) * kStBox;
                     }
                     tma_prefetch_2d(sq == 2 ? map[2] : sq == 1 ? map[1] : map[0], kq * kStBox, rq);
-                    if (a.rpad) tma_prefetch_2d(sq == 2 ? vtm[2] : sq == 1 ? vtm[1] : vtm[0], kq * kStBox, 0);
                 }
                 ++issued;
                 if (++s == a.nst) {
