@@ -505,13 +505,30 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
 static std::mutex g_pf_mu;
 static std::unordered_map<int, int> g_pf_attr;
 
+// Whether the persistent tiles kernel would leave most SMs idle: fewer output
+// tiles (128 tokens x about 224 rows) than half the SMs.  Each tile then runs
+// the whole K loop on one SM, and the split-K kernel, which spreads K over a
+// cluster, finishes sooner (measured on GB300: the large-set down projection at
+// 64 tokens, 24 tiles of 336 k-stages; the Gemma MLP at 16 to 128 tokens).
+static bool few_tiles(int64_t T, int64_t rows)
+{
+    wl_status s = WL_OK;
+    const DeviceInfo *di = device_info(&s);
+    if (!di) return false;
+    const int64_t tiles = (T + 127) / 128 * ((rows + 223) / 224);
+    return tiles * 2 < di->sm_count;
+}
+
 wl_status launch_prefill(const bf16 *x, const wl_proj *proj, int nproj, void *const *y, int64_t T,
                          int64_t in, int64_t Ktot, int64_t kmod, int64_t r, int ydt, cudaStream_t st)
 {
     bool valign = true;
-    for (int j = 0; j < nproj; ++j)
+    int64_t rows = 0;
+    for (int j = 0; j < nproj; ++j) {
         if (reinterpret_cast<uintptr_t>(proj[j].V) & 15) valign = false;
-    if (prefill_tiles_applicable(Ktot, r, ydt, false, valign))
+        rows += proj[j].out;
+    }
+    if (prefill_tiles_applicable(Ktot, r, ydt, false, valign) && !few_tiles(T, rows))
         return launch_prefill_tiles(x, proj, nproj, false, y, 0, T, in, Ktot, kmod, r, ydt, 0, 0, st);
     wl_status s = WL_OK;
     const DeviceInfo *di = device_info(&s);
@@ -652,7 +669,7 @@ wl_status launch_prefill_mlp(const bf16 *x, const wl_proj &gate, const wl_proj &
         return fail(WL_ERR_WORKSPACE, "MLP workspace too small for %lld tokens", (long long)T);
     char *w = static_cast<char *>(ws);
     const bool gu_valign = ((reinterpret_cast<uintptr_t>(gate.V) | reinterpret_cast<uintptr_t>(up.V)) & 15) == 0;
-    if (prefill_tiles_applicable(hidden, r, ydt, true, gu_valign)) {
+    if (prefill_tiles_applicable(hidden, r, ydt, true, gu_valign) && !few_tiles(T, 2 * inter)) {
         // gate and up in one persistent launch whose epilogue forms h, then down
         const int64_t kmod = (inter + kBKp - 1) / kBKp * kBKp;
         const int64_t ld = ydt == WL_OUT_F32 ? 2 * kmod : kmod;
