@@ -760,7 +760,8 @@ def measure_f32(dev, r=4, reps=10):
     encodings and devices"): fused Q/K/V of the Gemma-3-1B layer with fp32 x,
     W0, s, U, V.  T = 1: GB/s of algorithmic bytes (4-byte weights) against
     HBM; T = 2048: TFLOP/s against the fp32 CUDA-core peak.  CUDA-graph
-    replay over two weight sets (larger than L2 at T = 1 with 4 sets)."""
+    replay rotating weight sets: at T = 1 enough sets (7.1 MB each) to hold
+    twice the L2, so that W0 comes from HBM; at T = 2048 two sets."""
     import torch
     import rank_weight_reconstruction_wl_gb300 as wl
     import wl_synth
@@ -769,7 +770,9 @@ def measure_f32(dev, r=4, reps=10):
     h, q, kv = SHAPES["hidden"], SHAPES["q"], SHAPES["kv"]
     g = torch.Generator(device=dev)
     g.manual_seed(21)
-    sets = [[wl_synth.draw_theta_f32(g, h, o, r) for o in (q, kv, kv)] for _ in range(6)]
+    set_bytes = sum(4 * o * (h + 1 + 2 * r) for o in (q, kv, kv))
+    nsets = max(2, -(-2 * torch.cuda.get_device_properties(dev).L2_cache_size // set_bytes))
+    sets = [[wl_synth.draw_theta_f32(g, h, o, r) for o in (q, kv, kv)] for _ in range(nsets)]
     st = torch.cuda.Stream(dev)
     res = {"r": r, "peak_gbs": hbm_peak, "peak_kind": kind, "alu_peak_tflops": round(F32_ALU_PEAK_TFLOPS, 1),
            "alu_peak": "152 SMs x 128 fp32 lanes x 2 flops x 2.07 GHz (nominal, maximum clock)"}
@@ -799,7 +802,7 @@ def measure_f32(dev, r=4, reps=10):
         if T == 1:
             b = sum(4 * o * h + 4 * o + 4 * r * (h + o) for o in (q, kv, kv)) + 4 * T * (h + q + 2 * kv)
             res["T1"] = {"qkv_us": round(sec * 1e6, 2), "GBs": round(b / sec / 1e9, 1),
-                         "frac_of_hbm": round(b / sec / 1e9 / hbm_peak, 4)}
+                         "frac_of_hbm": round(b / sec / 1e9 / hbm_peak, 4), "weight_sets": len(use)}
         else:
             f = 2 * T * (h * (q + 2 * kv) + r * 3 * h + r * (q + 2 * kv))
             res["T2048"] = {"qkv_us": round(sec * 1e6, 1), "TFLOPs": round(f / sec / 1e12, 2),
@@ -950,9 +953,9 @@ def main():
                     help="stack kernel (one launch per 24 layers) or per-projection CUDA graph")
     ap.add_argument("--only-prefill", action="store_true",
                     help="run only the T=2048 prefill layer measurement (for profiling)")
-    ap.add_argument("--only", default=None, choices=["large1", "stack32", "materialize"],
+    ap.add_argument("--only", default=None, choices=["large1", "stack32", "materialize", "f32"],
                     help="run one measurement alone, for profiling: the large set at one token "
-                         "(one weight set), a 4-layer stack at 32 tokens, or wl_materialize")
+                         "(one weight set), a 4-layer stack at 32 tokens, wl_materialize, or the fp32 encoding")
     ap.add_argument("--layers", type=int, default=L_LAYERS,
                     help="layers in the stack (smaller values are for profiling only)")
     args = ap.parse_args()
@@ -982,6 +985,8 @@ def main():
         elif args.only == "stack32":
             res = measure_stack_grid(dev, steps=3, Ts=(32,), Gs=(L_LAYERS,), ranks=(args.rank,),
                                      nlayers=min(args.layers, 4))
+        elif args.only == "f32":
+            res = measure_f32(dev, r=args.rank)
         else:
             res = measure_materialize(dev, r=args.rank, nsets=1, reps=2)
         print(json.dumps({args.only: res}))

@@ -142,6 +142,176 @@ __global__ void __launch_bounds__(256) f32_linear_kernel(const __grid_constant__
     }
 }
 
+// ---------------------------------------------------------------- decode --
+// Few tokens (T <= 8): the call streams W0 once and the work per weight is
+// T multiply-adds, so the layout follows the weight stream instead of a GEMM
+// tile: one warp per output row reads the row with 16-byte loads (all of a
+// lane's loads in flight before the sums), x comes from L1.  z = x V is split
+// over a cluster of 8 CTAs by K (each CTA sums 1/8 of the rows of V), and every
+// CTA adds the 8 partial z in rank order from distributed shared memory, so all
+// rows of a projection see the same z.  A projection's CTAs are padded to a
+// multiple of 8 so that a cluster never spans two projections.
+constexpr int kF32DecRows = 8;   // output rows per CTA: one per warp
+constexpr int kF32DecCl = 8;     // CTAs per cluster
+constexpr int kF32DecZ = 64;     // T * r limit (z sums held per thread)
+
+__device__ __forceinline__ float ld_peer_f32(const float *p, uint32_t rank)
+{
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"((uint32_t)__cvta_generic_to_shared(p)), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(ra) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void f32_cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+template <int TT, int RR>
+__global__ void __cluster_dims__(kF32DecCl, 1, 1) __launch_bounds__(256)
+    f32_decode_kernel(const __grid_constant__ F32Args a)
+{
+    __shared__ float zred[8][kF32DecZ];  // per-warp partial z, then the CTA's partial (row 0)
+    __shared__ float zs[kF32DecZ];       // z of the projection: [t][k]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int cl = blockIdx.x / kF32DecCl;
+    const uint32_t crank = (uint32_t)(blockIdx.x % kF32DecCl);
+    // segment: seg.nt0 counts clusters
+    const int si = (a.nseg > 2 && cl >= a.seg[2].nt0) ? 2 : (a.nseg > 1 && cl >= a.seg[1].nt0) ? 1 : 0;
+    const F32Seg &sg = a.seg[si];
+    const int in = a.in, r = a.r;
+    const int o = ((cl - sg.nt0) * kF32DecCl + (int)crank) * kF32DecRows + warp;
+    const bool row_ok = o < sg.out;
+    const float *__restrict__ x = a.x;
+
+    // this warp's row: the first loads in flight before z
+    const float4 *wrow = reinterpret_cast<const float4 *>(sg.W0 + (int64_t)(row_ok ? o : 0) * in);
+    const int nq = in >> 2;  // float4 per row
+    float dot[TT];
+#pragma unroll
+    for (int t = 0; t < TT; ++t) dot[t] = 0.f;
+    constexpr int PF = 8;
+    float4 wq[PF];
+#pragma unroll
+    for (int u = 0; u < PF; ++u) wq[u] = (row_ok && lane + 32 * u < nq) ? __ldg(wrow + lane + 32 * u) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    if (RR > 0) {
+        // z partial over this CTA's eighth of K: thread rows i = k0 + tid, + 256, ...
+        const int k0 = (int)(((int64_t)in * crank) / kF32DecCl), k1 = (int)(((int64_t)in * (crank + 1)) / kF32DecCl);
+        constexpr int RA = RR > 0 ? RR : 1;
+        float zp[TT][RA];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int k = 0; k < RR; ++k) zp[t][k] = 0.f;
+        for (int i = k0 + tid; i < k1; i += 256) {
+            const float *vr = sg.V + (int64_t)i * r;
+            float vv[RA];
+#pragma unroll
+            for (int k = 0; k < RR; ++k) vv[k] = k < r ? __ldg(vr + k) : 0.f;
+#pragma unroll
+            for (int t = 0; t < TT; ++t) {
+                const float xv = t < a.T ? __ldg(x + (int64_t)t * in + i) : 0.f;
+#pragma unroll
+                for (int k = 0; k < RR; ++k) zp[t][k] = fmaf(xv, vv[k], zp[t][k]);
+            }
+        }
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+#pragma unroll
+            for (int k = 0; k < RR; ++k) {
+                float v = zp[t][k];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+                if (lane == 0) zred[warp][t * RR + k] = v;
+            }
+        __syncthreads();
+        if (tid < TT * RR) {
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < 8; ++w) v += zred[w][tid];
+            zred[0][tid] = v;  // this CTA's partial (row 0 is read by the cluster)
+        }
+        f32_cluster_sync();
+        if (tid < TT * RR) {
+            float v = 0.f;
+            for (uint32_t c = 0; c < (uint32_t)kF32DecCl; ++c) v += ld_peer_f32(&zred[0][tid], c);
+            zs[tid] = v;
+        }
+        // no CTA leaves (or rewrites zred) before every CTA has read it
+        f32_cluster_sync();
+    }
+
+    // the row's dot products with x
+    for (int q0 = 0; q0 < nq; q0 += 32 * PF) {
+#pragma unroll
+        for (int u = 0; u < PF; ++u) {
+            const int q = q0 + lane + 32 * u;
+            if (q < nq) {
+                const float4 w = wq[u];
+#pragma unroll
+                for (int t = 0; t < TT; ++t) {
+                    if (t < a.T) {
+                        const float4 xv = __ldg(reinterpret_cast<const float4 *>(x + (int64_t)t * in) + q);
+                        dot[t] = fmaf(w.x, xv.x, dot[t]);
+                        dot[t] = fmaf(w.y, xv.y, dot[t]);
+                        dot[t] = fmaf(w.z, xv.z, dot[t]);
+                        dot[t] = fmaf(w.w, xv.w, dot[t]);
+                    }
+                }
+            }
+            const int qn = q + 32 * PF;
+            wq[u] = (row_ok && qn < nq) ? __ldg(wrow + qn) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TT; ++t)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) dot[t] += __shfl_xor_sync(0xffffffffu, dot[t], off);
+    if (!row_ok) return;
+    // lane t writes token t
+#pragma unroll
+    for (int t = 0; t < TT; ++t) {
+        if (lane == t && t < a.T) {
+            float v = sg.s[o] * dot[t];
+            if (RR > 0)
+                for (int k = 0; k < r; ++k) v = fmaf(sg.U[(int64_t)o * r + k], zs[t * RR + k], v);
+            store_out(sg.y, a.ydt, (int64_t)t * sg.out + o, v);
+        }
+    }
+}
+
+typedef void (*f32_dec_fn)(F32Args);
+
+template <int TT>
+static f32_dec_fn pick_dec_rank(int r)
+{
+    if (r == 0) return f32_decode_kernel<TT, 0>;
+    if (r <= 4) return f32_decode_kernel<TT, 4>;
+    if (r <= 8 && TT * 8 <= kF32DecZ) return f32_decode_kernel<TT, (TT * 8 <= kF32DecZ ? 8 : 4)>;
+    if (r <= 16 && TT * 16 <= kF32DecZ) return f32_decode_kernel<TT, (TT * 16 <= kF32DecZ ? 16 : 4)>;
+    if (r <= 32 && TT * 32 <= kF32DecZ) return f32_decode_kernel<TT, (TT * 32 <= kF32DecZ ? 32 : 4)>;
+    if (r <= 64 && TT * 64 <= kF32DecZ) return f32_decode_kernel<TT, (TT * 64 <= kF32DecZ ? 64 : 4)>;
+    return nullptr;
+}
+
+static f32_dec_fn pick_dec(int64_t T, int64_t r)
+{
+    switch (T) {
+    case 1: return pick_dec_rank<1>((int)r);
+    case 2: return pick_dec_rank<2>((int)r);
+    case 3:
+    case 4: return pick_dec_rank<4>((int)r);
+    case 5:
+    case 6:
+    case 7:
+    case 8: return pick_dec_rank<8>((int)r);
+    default: return nullptr;
+    }
+}
+
 typedef void (*f32_fn)(F32Args);
 
 template <int BM, int BN, int BK, int TM, int TN>
@@ -159,6 +329,33 @@ static f32_fn pick_rank(int r)
 wl_status launch_f32_linear(const float *x, const wl_proj_f32 *proj, int nproj, void *const *y, int64_t T,
                             int64_t in, int64_t r, int ydt, cudaStream_t st)
 {
+    // few tokens: the weight-streaming form (16-byte rows: in a multiple of 4)
+    const f32_dec_fn dfn = (in % 4 == 0) ? pick_dec(T, r) : nullptr;
+    if (dfn) {
+        F32Args a = {};
+        a.x = x;
+        a.T = (int)T;
+        a.in = (int)in;
+        a.r = (int)r;
+        a.ydt = ydt;
+        a.nseg = nproj;
+        int ncl = 0;
+        for (int j = 0; j < nproj; ++j) {
+            F32Seg &sg = a.seg[j];
+            sg.W0 = proj[j].W0;
+            sg.s = proj[j].s;
+            sg.U = proj[j].U;
+            sg.V = proj[j].V;
+            sg.y = y[j];
+            sg.out = (int)proj[j].out;
+            sg.nt0 = ncl;
+            ncl += (int)((proj[j].out + kF32DecRows * kF32DecCl - 1) / (kF32DecRows * kF32DecCl));
+        }
+        dfn<<<ncl * kF32DecCl, 256, 0, st>>>(a);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "fp32 decode launch");
+        return WL_OK;
+    }
     const bool small = T <= 16;
     const int BM = small ? 16 : 64, BN = small ? 32 : 128;
     F32Args a = {};
