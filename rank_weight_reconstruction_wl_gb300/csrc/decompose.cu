@@ -82,24 +82,30 @@ __global__ void dc_scale_kernel(const bf16 *__restrict__ W, const bf16 *__restri
 // TR = 1:  C[m, j] = sum_t R[t, m] B[t, j]   (Z = R^T Y; m < in,  t < out)
 // with R[o, i] = W[o, i] - s[o] W0[o, i].  B [nt, k] and C [nm, k] fp32
 // row-major.  CTA: 32 values of m x all k columns, 16 x 16 threads (2 m x
-// KT columns each), the contraction in chunks of 32.
+// KT columns each), the contraction in chunks of 32.  The contraction is
+// split over blockIdx.y (tsplit rows of t each): split q writes its partial
+// sums to C + q nm k, summed afterwards in split order (dc_sum_splits), so
+// that the result does not depend on timing.
 template <int TR, int KT>
 __global__ void __launch_bounds__(256) dc_rmul_kernel(const bf16 *__restrict__ W, const bf16 *__restrict__ W0,
                                                       const float *__restrict__ s, const float *__restrict__ B,
-                                                      float *__restrict__ C, int out, int in, int k)
+                                                      float *__restrict__ C, int out, int in, int k, int tsplit)
 {
     constexpr int BM = 32, BK = 32, KP = 16 * KT;
     __shared__ __align__(16) float As[BK][BM + 1];
     __shared__ __align__(16) float Bs[BK][KP + 4];
     const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-    const int nm = TR ? in : out, nt = TR ? out : in;
+    const int nm = TR ? in : out;
     const int m0 = blockIdx.x * BM;
+    const int tb = blockIdx.y * tsplit;
+    const int nt = min(TR ? out : in, tb + tsplit);
+    C += (size_t)blockIdx.y * nm * k;
     float acc[2][KT];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
         for (int b = 0; b < KT; ++b) acc[a][b] = 0.f;
-    for (int t0 = 0; t0 < nt; t0 += BK) {
+    for (int t0 = tb; t0 < nt; t0 += BK) {
         for (int e = tid; e < BM * BK; e += 256) {
             int m, t;
             if (TR) {  // rows o = t of R, consecutive threads along i = m
@@ -147,19 +153,55 @@ __global__ void __launch_bounds__(256) dc_rmul_kernel(const bf16 *__restrict__ W
     }
 }
 
+// C[e] = sum over q < nsplit of P[q n + e], in q order
+__global__ void dc_sum_splits_kernel(const float *__restrict__ P, int nsplit, int64_t n, float *__restrict__ C)
+{
+    for (int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; e < n; e += (int64_t)gridDim.x * blockDim.x) {
+        float v = 0.f;
+        for (int q = 0; q < nsplit; ++q) v += P[(size_t)q * n + e];
+        C[e] = v;
+    }
+}
+
 // ---- Gram matrices Y^T Y (k x k) of a tall Y [n, k] -----------------------
 // partial Gram of rows [blockIdx.x * rows, ...) per CTA, then a fixed-order sum
+// (rows staged through shared memory 32 at a time, read coalesced; a
+// thread's entries summed over the rows in order)
+constexpr int kGramChunk = 32;
+constexpr int kGramRows = 64;  // rows of Y per CTA (partial Gram matrices: n / 64 of them)
+template <int EPT>  // entries per thread: k * k <= 256 * EPT
 __global__ void __launch_bounds__(256) dc_gram_partial_kernel(const float *__restrict__ Y, int n, int k, int rows,
                                                               float *__restrict__ part)
 {
+    extern __shared__ float ys[];  // [kGramChunk][k]
     const int r0 = blockIdx.x * rows, r1 = min(n, r0 + rows);
     float *P = part + (size_t)blockIdx.x * k * k;
-    for (int e = threadIdx.x; e < k * k; e += blockDim.x) {
-        const int a = e / k, b = e - a * k;
-        float v = 0.f;
-        if (b >= a)
-            for (int i = r0; i < r1; ++i) v = fmaf(Y[(int64_t)i * k + a], Y[(int64_t)i * k + b], v);
-        P[e] = v;
+    float v[EPT];
+    const int ne = k * k;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) v[j] = 0.f;
+    for (int c0 = r0; c0 < r1; c0 += kGramChunk) {
+        const int nr = min(kGramChunk, r1 - c0);
+        __syncthreads();
+        for (int e = threadIdx.x; e < nr * k; e += blockDim.x) ys[e] = Y[(int64_t)c0 * k + e];
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < EPT; ++j) {
+            const int e = threadIdx.x + j * 256;
+            if (e < ne) {
+                const int a = e / k, b = e - a * k;
+                if (b >= a) {
+                    float acc = v[j];
+                    for (int i = 0; i < nr; ++i) acc = fmaf(ys[i * k + a], ys[i * k + b], acc);
+                    v[j] = acc;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+        const int e = threadIdx.x + j * 256;
+        if (e < ne) P[e] = v[j];
     }
 }
 
@@ -354,9 +396,16 @@ __global__ void __launch_bounds__(256) dc_apply_kernel(const float *__restrict__
 
 // ------------------------------------------------------------------ host
 struct DcWs {
-    float *Y, *Y2, *Z, *Z2, *part, *G, *M, *MU, *MV;
+    float *Y, *Y2, *Z, *Z2, *part, *G, *M, *MU, *MV, *split;
     int nparts;
+    int64_t split_floats;
 };
+
+// Partial sums of the split contraction: up to 16 splits, at most 8 Mi floats.
+static int64_t dc_split_floats(int64_t out, int64_t in, int64_t k)
+{
+    return std::min<int64_t>(16 * std::max(out, in) * k, (int64_t)1 << 23);
+}
 
 static size_t dc_carve(int64_t out, int64_t in, int64_t k, int64_t r, char *base, DcWs *w)
 {
@@ -367,11 +416,15 @@ static size_t dc_carve(int64_t out, int64_t in, int64_t k, int64_t r, char *base
         off += bytes;
         return o;
     };
-    const int nparts = (int)((std::max(out, in) + 255) / 256);
+    const int nparts = (int)((std::max(out, in) + kGramRows - 1) / kGramRows);
     const size_t oY = take(4 * out * k), oY2 = take(4 * out * k), oZ = take(4 * in * k), oZ2 = take(4 * in * k);
     const size_t oP = take(4 * (size_t)nparts * k * k), oG = take(4 * k * k), oM = take(4 * k * k);
     const size_t oMU = take(4 * k * r), oMV = take(4 * k * r);
+    const int64_t nsplit_f = dc_split_floats(out, in, k);
+    const size_t oS = take(4 * (size_t)nsplit_f);
     if (base) {
+        w->split = reinterpret_cast<float *>(base + oS);
+        w->split_floats = nsplit_f;
         w->Y = reinterpret_cast<float *>(base + oY);
         w->Y2 = reinterpret_cast<float *>(base + oY2);
         w->Z = reinterpret_cast<float *>(base + oZ);
@@ -393,27 +446,49 @@ size_t decompose_workspace_bytes(int64_t out, int64_t in, int64_t r, int64_t p)
 
 static int kt_of(int k) { return k <= 16 ? 1 : k <= 32 ? 2 : k <= 64 ? 4 : k <= 96 ? 6 : k <= 128 ? 8 : 10; }
 
+// The contraction is split so that the grid holds about four CTAs per SM
+// (the m strips alone are too few where m runs over the shorter side), each
+// split a multiple of 32 rows of t, within the workspace's partial buffer.
 template <int TR>
 static void rmul(const bf16 *W, const bf16 *W0, const float *s, const float *B, float *C, int out, int in, int k,
-                 cudaStream_t st)
+                 const DcWs &w, const DeviceInfo *di, cudaStream_t st)
 {
-    const int nm = TR ? in : out;
-    const dim3 grid((unsigned)((nm + 31) / 32));
+    const int nm = TR ? in : out, nt = TR ? out : in;
+    const int mt = (nm + 31) / 32;
+    int nsplit = std::max(1, (4 * di->sm_count + mt - 1) / mt);
+    nsplit = std::min(nsplit, (nt + 31) / 32);
+    nsplit = (int)std::min<int64_t>(nsplit, std::max<int64_t>(1, w.split_floats / ((int64_t)nm * k)));
+    int tsplit = (nt + nsplit - 1) / nsplit;
+    tsplit = (tsplit + 31) / 32 * 32;
+    nsplit = (nt + tsplit - 1) / tsplit;
+    float *dst = nsplit > 1 ? w.split : C;
+    const dim3 grid((unsigned)mt, (unsigned)nsplit);
     switch (kt_of(k)) {
-    case 1: dc_rmul_kernel<TR, 1><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
-    case 2: dc_rmul_kernel<TR, 2><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
-    case 4: dc_rmul_kernel<TR, 4><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
-    case 6: dc_rmul_kernel<TR, 6><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
-    case 8: dc_rmul_kernel<TR, 8><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
-    default: dc_rmul_kernel<TR, 10><<<grid, 256, 0, st>>>(W, W0, s, B, C, out, in, k); break;
+    case 1: dc_rmul_kernel<TR, 1><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    case 2: dc_rmul_kernel<TR, 2><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    case 4: dc_rmul_kernel<TR, 4><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    case 6: dc_rmul_kernel<TR, 6><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    case 8: dc_rmul_kernel<TR, 8><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    default: dc_rmul_kernel<TR, 10><<<grid, 256, 0, st>>>(W, W0, s, B, dst, out, in, k, tsplit); break;
+    }
+    if (nsplit > 1) {
+        const int64_t n = (int64_t)nm * k;
+        dc_sum_splits_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4 * di->sm_count), 256, 0, st>>>(
+            w.split, nsplit, n, C);
     }
 }
 
 static void gram(const float *Y, int n, int k, const DcWs &w, cudaStream_t st)
 {
-    const int rows = 256;
+    const int rows = kGramRows;
     const int parts = (n + rows - 1) / rows;
-    dc_gram_partial_kernel<<<parts, 256, 0, st>>>(Y, n, k, rows, w.part);
+    const size_t sm = (size_t)kGramChunk * k * 4;
+    if (k * k <= 256 * 4)
+        dc_gram_partial_kernel<4><<<parts, 256, sm, st>>>(Y, n, k, rows, w.part);
+    else if (k * k <= 256 * 16)
+        dc_gram_partial_kernel<16><<<parts, 256, sm, st>>>(Y, n, k, rows, w.part);
+    else
+        dc_gram_partial_kernel<100><<<parts, 256, sm, st>>>(Y, n, k, rows, w.part);
     dc_gram_reduce_kernel<<<(k * k + 255) / 256, 256, 0, st>>>(w.part, parts, k, w.G);
 }
 
@@ -462,15 +537,15 @@ wl_status launch_decompose(const bf16 *const *Wl, int n, int out, int in, int r,
         dc_scale_kernel<<<(out + 7) / 8, 256, 0, st>>>(Wl[l], W0, out, in, sl);
         if (r == 0) continue;
         float *Y = w.Y, *Y2 = w.Y2, *Z = w.Z, *Z2 = w.Z2;
-        rmul<0>(Wl[l], W0, sl, omega, Y, out, in, k, st);  // Y = R Omega
+        rmul<0>(Wl[l], W0, sl, omega, Y, out, in, k, w, di, st);  // Y = R Omega
         orth(&Y, &Y2, out, k, w, di, st);
         for (int it = 0; it < iters; ++it) {
-            rmul<1>(Wl[l], W0, sl, Y, Z, out, in, k, st);  // Z = R^T Q
+            rmul<1>(Wl[l], W0, sl, Y, Z, out, in, k, w, di, st);  // Z = R^T Q
             orth(&Z, &Z2, in, k, w, di, st);
-            rmul<0>(Wl[l], W0, sl, Z, Y, out, in, k, st);  // Y = R Z
+            rmul<0>(Wl[l], W0, sl, Z, Y, out, in, k, w, di, st);  // Y = R Z
             orth(&Y, &Y2, out, k, w, di, st);
         }
-        rmul<1>(Wl[l], W0, sl, Y, Z, out, in, k, st);  // B^T = R^T Q
+        rmul<1>(Wl[l], W0, sl, Y, Z, out, in, k, w, di, st);  // B^T = R^T Q
         gram(Z, in, k, w, st);                          // B B^T
         dc_small_kernel<<<1, 1024, small_smem(k), st>>>(w.G, k, r, 1, w.M, w.MU, w.MV, di->status);
         const int64_t nu = (int64_t)out * r, nv = (int64_t)in * r;
