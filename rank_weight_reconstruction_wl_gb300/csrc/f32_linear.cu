@@ -312,7 +312,169 @@ static f32_dec_fn pick_dec(int64_t T, int64_t r)
     }
 }
 
+// ------------------------------------------------------------ many tokens --
+// 128 tokens x 64 rows per CTA, 8 x 4 outputs per thread (16 x 16 threads),
+// K in steps of 16 through two shared-memory buffers: the next step's x (two
+// 16-byte loads per thread), W0 (one) and V rows are fetched into registers
+// while the current step is multiplied, then stored to the other buffer, one
+// barrier per step.  x and W0 tiles are stored k-major (transposed), so a
+// thread reads its 8 tokens as two 16-byte words, its 4 rows as one.  z of
+// the tile's tokens (8 tokens x ZTN ranks per thread) comes from the same x
+// words.  The sums over k run in order, as in the form above.
+constexpr int kGBM = 128, kGBN = 64, kGBK = 16;
+
+template <int ZTN>
+__global__ void __launch_bounds__(256, ZTN >= 4 ? 1 : 2) f32_gemm_kernel(const __grid_constant__ F32Args a)
+{
+    constexpr int RP = 16 * ZTN;  // padded ranks
+    constexpr int AS = kGBM + 4, BS = kGBN + 4, VSS = RP + 4, ZS = RP + 1;
+    constexpr int STAGE_F = kGBK * (AS + BS + VSS);
+    constexpr int Z_F = kGBM * ZS;
+    __shared__ __align__(16) float smf[2 * STAGE_F > Z_F ? 2 * STAGE_F : Z_F];
+    const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+    const int nt = blockIdx.x;
+    const int si = (a.nseg > 2 && nt >= a.seg[2].nt0) ? 2 : (a.nseg > 1 && nt >= a.seg[1].nt0) ? 1 : 0;
+    const F32Seg &sg = a.seg[si];
+    const float *__restrict__ W0 = sg.W0;
+    const float *__restrict__ V = sg.V;
+    const float *__restrict__ x = a.x;
+    const int out = sg.out, in = a.in, T = a.T, r = a.r;
+    const int o0 = (nt - sg.nt0) * kGBN;
+    const int t0 = blockIdx.y * kGBM;
+
+    // this thread's loads of a step: x row lr (tokens), k words kq..kq+3 and
+    // kq+8..kq+11; W0 row wr, k words wq..wq+3
+    const int lr = tid >> 1, kq = (tid & 1) * 4;
+    const int wr = tid >> 2, wq = (tid & 3) * 4;
+    const bool xok = t0 + lr < T, wok = o0 + wr < out;
+    const float *xp = x + (int64_t)(xok ? t0 + lr : 0) * in + kq;
+    const float *wp = W0 + (int64_t)(wok ? o0 + wr : 0) * in + wq;
+    // V rows of a step: RP ranks x 16 k, (16 * RP) / 256 values per thread
+    constexpr int VPT = (kGBK * RP + 255) / 256;
+
+    float acc[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+    float zacc[8][ZTN > 0 ? ZTN : 1];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < (ZTN > 0 ? ZTN : 1); ++j) zacc[i][j] = 0.f;
+
+    auto load = [&](int k0, float4 (&xa)[2], float4 &wa, float (&vr)[VPT > 0 ? VPT : 1]) {
+        // in % 8 == 0: a word of 4 is all in or all out
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            xa[h] = (xok && k0 + 8 * h + kq < in) ? __ldg(reinterpret_cast<const float4 *>(xp + k0 + 8 * h))
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+        wa = (wok && k0 + wq < in) ? __ldg(reinterpret_cast<const float4 *>(wp + k0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (ZTN > 0) {
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const int e = tid + 256 * u, k = e / RP, j = e - k * RP;
+                vr[u] = (e < kGBK * RP && j < r && k0 + k < in) ? __ldg(V + (int64_t)(k0 + k) * r + j) : 0.f;
+            }
+        }
+    };
+    auto store = [&](int b, const float4 (&xa)[2], const float4 &wa, const float (&vr)[VPT > 0 ? VPT : 1]) {
+        float *As = smf + b * STAGE_F, *Bs = As + kGBK * AS, *Vs = Bs + kGBK * BS;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int kk = kq + 8 * h;
+            As[(kk + 0) * AS + lr] = xa[h].x;
+            As[(kk + 1) * AS + lr] = xa[h].y;
+            As[(kk + 2) * AS + lr] = xa[h].z;
+            As[(kk + 3) * AS + lr] = xa[h].w;
+        }
+        Bs[(wq + 0) * BS + wr] = wa.x;
+        Bs[(wq + 1) * BS + wr] = wa.y;
+        Bs[(wq + 2) * BS + wr] = wa.z;
+        Bs[(wq + 3) * BS + wr] = wa.w;
+        if (ZTN > 0) {
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) {
+                const int e = tid + 256 * u, k = e / RP, j = e - k * RP;
+                if (e < kGBK * RP) Vs[k * VSS + j] = vr[u];
+            }
+        }
+    };
+
+    float4 xa[2], wa;
+    float vr[VPT > 0 ? VPT : 1];
+    load(0, xa, wa, vr);
+    store(0, xa, wa, vr);
+    __syncthreads();
+    int b = 0;
+    for (int k0 = 0; k0 < in; k0 += kGBK) {
+        const bool more = k0 + kGBK < in;
+        if (more) load(k0 + kGBK, xa, wa, vr);
+        const float *As = smf + b * STAGE_F, *Bs = As + kGBK * AS, *Vs = Bs + kGBK * BS;
+#pragma unroll
+        for (int k = 0; k < kGBK; ++k) {
+            const float4 a0 = *reinterpret_cast<const float4 *>(As + k * AS + ty * 8);
+            const float4 a1 = *reinterpret_cast<const float4 *>(As + k * AS + ty * 8 + 4);
+            const float4 b0 = *reinterpret_cast<const float4 *>(Bs + k * BS + tx * 4);
+            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+            const float bv[4] = {b0.x, b0.y, b0.z, b0.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+            if (ZTN > 0) {
+#pragma unroll
+                for (int j = 0; j < ZTN; ++j) {
+                    const float zv = Vs[k * VSS + tx * ZTN + j];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) zacc[i][j] = fmaf(av[i], zv, zacc[i][j]);
+                }
+            }
+        }
+        if (more) store(b ^ 1, xa, wa, vr);
+        __syncthreads();
+        b ^= 1;
+    }
+
+    // z of the tile's tokens, then y = s * acc + U z
+    float(*zs)[ZS] = reinterpret_cast<float(*)[ZS]>(smf);
+    if (ZTN > 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+#pragma unroll
+            for (int j = 0; j < ZTN; ++j) zs[ty * 8 + i][tx * ZTN + j] = zacc[i][j];
+        __syncthreads();
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int o = o0 + tx * 4 + j;
+        if (o >= out) continue;
+        const float sv = sg.s[o];
+        const float *Ur = sg.U + (int64_t)o * r;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int tl = ty * 8 + i, t = t0 + tl;
+            if (t >= T) continue;
+            float v = sv * acc[i][j];
+            if (ZTN > 0)
+                for (int k = 0; k < r; ++k) v = fmaf(Ur[k], zs[tl][k], v);
+            store_out(sg.y, a.ydt, (int64_t)t * out + o, v);
+        }
+    }
+}
+
 typedef void (*f32_fn)(F32Args);
+
+// ranks up to 64 (above, the tiled form: the z stash of 128 tokens would
+// not fit the static shared memory)
+static f32_fn pick_gemm(int r)
+{
+    if (r == 0) return f32_gemm_kernel<0>;
+    if (r <= 16) return f32_gemm_kernel<1>;
+    if (r <= 32) return f32_gemm_kernel<2>;
+    if (r <= 64) return f32_gemm_kernel<4>;
+    return nullptr;
+}
 
 template <int BM, int BN, int BK, int TM, int TN>
 static f32_fn pick_rank(int r)
@@ -357,7 +519,8 @@ wl_status launch_f32_linear(const float *x, const wl_proj_f32 *proj, int nproj, 
         return WL_OK;
     }
     const bool small = T <= 16;
-    const int BM = small ? 16 : 64, BN = small ? 32 : 128;
+    const bool gemm = !small && r <= 64;
+    const int BM = small ? 16 : gemm ? kGBM : 64, BN = small ? 32 : gemm ? kGBN : 128;
     F32Args a = {};
     a.x = x;
     a.T = (int)T;
@@ -380,7 +543,8 @@ wl_status launch_f32_linear(const float *x, const wl_proj_f32 *proj, int nproj, 
     const int64_t mt = (T + BM - 1) / BM;
     if (mt > 65535) return fail(WL_ERR_UNSUPPORTED, "fp32 linear: T too large (%lld)", (long long)T);
     const dim3 grid((unsigned)ntiles, (unsigned)mt);
-    const f32_fn fn = small ? pick_rank<16, 32, 32, 1, 2>((int)r) : pick_rank<64, 128, 16, 4, 8>((int)r);
+    const f32_fn fn = small ? pick_rank<16, 32, 32, 1, 2>((int)r)
+                            : gemm ? pick_gemm((int)r) : pick_rank<64, 128, 16, 4, 8>((int)r);
     fn<<<grid, 256, 0, st>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "fp32 linear launch");

@@ -22,6 +22,8 @@ def _to(th, dev):
     (17, 512, 130, 16), (64, 1152, 256, 128), (200, 200, 72, 33), (7, 6912, 1152, 4),
     # the few-token form at each of its z widths: T x r up to 64
     (1, 5376, 4096, 64), (2, 1152, 1536, 32), (8, 1024, 1152, 8), (4, 2056, 300, 16), (1, 16, 9, 3),
+    # the 128 x 128 tiled form at each of its z widths, ragged T, out and K
+    (40, 128, 72, 0), (33, 1024, 200, 24), (130, 264, 260, 64),
 ])
 @pytest.mark.parametrize("ydt", [torch.float32, torch.bfloat16])
 def test_f32_linear_ragged(wl, orc, gpu, T, n_in, out, r, ydt):
