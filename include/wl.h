@@ -21,7 +21,14 @@
  *  Memory: every pointer is device memory owned by the caller.  The library
  *    allocates nothing in these calls.  Outputs must not alias inputs.
  *  Streams: `stream` is a cudaStream_t (NULL = legacy default stream).  Calls
- *    are asynchronous on that stream; results are ready when it is.
+ *    are asynchronous on that stream; results are ready when it is.  The
+ *    decode-size launches (wl_linear, wl_qkv_fused, wl_mlp_geglu_fused at
+ *    T <= 8) use programmatic dependent launch: they start streaming W0, s,
+ *    U and V while the previous kernel on the stream finishes, and read x
+ *    (and write y) only after it has completed.  So the weights must not be
+ *    written by the kernel launched immediately before the call on the same
+ *    stream; weights written by a copy (cudaMemcpy*), on another stream
+ *    joined by an event, or by any earlier kernel are fine.
  *  Errors: return codes only; nothing is thrown or aborted across the ABI.
  *    Arguments are checked before anything is launched; on error nothing is
  *    launched and wl_last_error() describes the failure.  A failed launch
