@@ -191,5 +191,9 @@ def materialize_layers(layers: list[LayerTheta], dt=torch.bfloat16) -> list[Laye
                                        torch.zeros(o, 0, dtype=torch.bfloat16, device=W.device),
                                        torch.zeros(i, 0, dtype=torch.bfloat16, device=W.device))
         out.append(LayerTheta(**fams))
+    # the decode launches read weights while the previous kernel on the stream
+    # finishes: the bundles are complete before any of them runs
+    if out:
+        torch.cuda.current_stream(out[0].q.W0.device).synchronize()
     return out
 
