@@ -424,6 +424,32 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 vtm[j] = a.ph[phi].seg[j].vtmap;
                 rt0[j] = j < nseg ? a.ph[phi].seg[j].rt0 : 0x7fffffff;
             }
+            // Every box of the phase beyond one ring's worth, into L2 now: the
+            // producer reaches a phase while the consumers are still on the
+            // previous one or waiting for its partial sums, when HBM has little
+            // else to do; the ring's refill for those boxes then comes from L2.
+            // Only W0, and only with a ring of 16 stages or more: with a short
+            // ring (large ranks) the extra copies cost more than they save.
+            if (a.nst >= 16 && b1 - b0 > a.nst) {
+                int rtq = (b0 + a.nst) / bpr, wq = (b0 + a.nst) - rtq * bpr;
+                for (int bq = b0 + a.nst; bq < b1; ++bq) {
+                    int sq, kq, rq;
+                    if (gu) {
+                        sq = wq >= KB ? 1 : 0;
+                        kq = wq - sq * KB;
+                        rq = rtq * kStBox;
+                    } else {
+                        sq = rtq >= rt0[2] ? 2 : (rtq >= rt0[1] ? 1 : 0);
+                        kq = wq;
+                        rq = (rtq - (sq == 2 ? rt0[2] : sq == 1 ? rt0[1] : 0)) * kStBox;
+                    }
+                    tma_prefetch_2d(sq == 2 ? map[2] : sq == 1 ? map[1] : map[0], kq * kStBox, rq);
+                    if (++wq == bpr) {
+                        wq = 0;
+                        ++rtq;
+                    }
+                }
+            }
             int rt = b0 / bpr, w = b0 - rt * bpr;
             for (int b = b0; b < b1; ++b) {
                 // segment, row offset and k block of box (rt, w)
@@ -448,25 +474,6 @@ __global__ void __launch_bounds__(kStThreads, 1) stack_kernel(const __grid_const
                 const uint32_t sdst = w_base + (uint32_t)s * (uint32_t)sbytes_stage;
                 tma_load_2d_u32(sdst, m, kb * kStBox, row0, fb);
                 if (a.rpad) tma_load_2d_u32(sdst + kStBoxBytes, vm, kb * kStBox, 0, fb);
-                // the box one ring ahead in this phase, into L2: when the
-                // ring is full at the phase's start, its refill then comes
-                // from L2 instead of HBM.  Only W0, and only with a ring of 16
-                // stages or more: with a short ring (large ranks) the extra
-                // copies cost the producer more than they save.
-                if (a.nst >= 16 && b + a.nst < b1) {
-                    const int bq = b + a.nst, rtq = bq / bpr, wq = bq - rtq * bpr;
-                    int sq, kq, rq;
-                    if (gu) {
-                        sq = wq >= KB ? 1 : 0;
-                        kq = wq - sq * KB;
-                        rq = rtq * kStBox;
-                    } else {
-                        sq = rtq >= rt0[2] ? 2 : (rtq >= rt0[1] ? 1 : 0);
-                        kq = wq;
-                        rq = (rtq - (sq == 2 ? rt0[2] : sq == 1 ? rt0[1] : 0)) * kStBox;
-                    }
-                    tma_prefetch_2d(sq == 2 ? map[2] : sq == 1 ? map[1] : map[0], kq * kStBox, rq);
-                }
                 ++issued;
                 if (++s == a.nst) {
                     s = 0;
