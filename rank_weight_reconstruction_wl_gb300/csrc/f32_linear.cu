@@ -7,13 +7,17 @@
 //
 // fp32 inputs keep fp32 arithmetic: the bf16 tensor-core forms would round
 // every operand to 8 significant bits, far outside the fp32 output tolerance,
-// and the fp32 tensor-core form (tf32) keeps only 11.  So this is a tiled
-// CUDA-core GEMM with fp32 FMAs: a CTA computes a BM-token x BN-row tile of y
-// over the whole K, staging x, W0 and the matching V rows through shared
-// memory BK columns at a time; z of the CTA's tokens is accumulated in the
-// same K loop (the x tile is already staged), and the epilogue applies the
-// scale and U z.  One launch per call; Q/K/V are segments of one grid, so x
-// is read once per token tile.
+// and the fp32 tensor-core form (tf32) keeps only 11.  So these are CUDA-core
+// kernels with fp32 FMAs, one launch per call, Q/K/V as segments of one grid:
+//   T <= 8 (T r <= 64): f32_decode_kernel, shaped by the weight stream (a
+//     warp per output row, z split over a cluster of 8 CTAs);
+//   more tokens, r <= 64: f32_gemm_kernel, a double-buffered 128-token x
+//     64-row tile;
+//   otherwise f32_linear_kernel: a CTA computes a BM-token x BN-row tile of y
+//     over the whole K, staging x, W0 and the matching V rows through shared
+//     memory BK columns at a time.
+// In the tiled forms z of the CTA's tokens is accumulated in the same K loop
+// (the x tile is already staged), and the epilogue applies the scale and U z.
 #include "wl_internal.cuh"
 
 namespace wl {
