@@ -49,7 +49,9 @@ def test_passthrough_exact(wl, gpu, r):
         assert not U.float().abs().sum() and not V.float().abs().sum()
 
 
-@pytest.mark.parametrize("out,inp,r,n", [(96, 160, 4, 2), (130, 72, 8, 2), (256, 512, 16, 3), (6912, 1152, 16, 2)])
+@pytest.mark.parametrize("out,inp,r,n", [(96, 160, 4, 2), (130, 72, 8, 2), (256, 512, 16, 3), (6912, 1152, 16, 2),
+                                         # k = r + p of 48 and 108: the wider Gram forms
+                                         (160, 256, 40, 2), (300, 264, 100, 2)])
 def test_planted_residual_matches_oracle(wl, orc, gpu, out, inp, r, n):
     from oracle import decompose as D
 
